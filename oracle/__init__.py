@@ -1,0 +1,154 @@
+"""SiTU-GLU oracle: plain fp64 CPU restatement of the method (test infrastructure).
+
+Only ``tests/``, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline and
+reference legs may import this package. The product path (``bwd_situ_glu_gb300``)
+never imports it, and the two share no code.
+
+The arithmetic lives in ``situ_glu_oracle.c`` (plain C, double, libm), which
+states the formulas and cites the passages they come from:
+
+* "Frontier-scale RL with Kimi K3", section "Streaming activations":
+  the forward definition ``situ_and_mul``.
+* "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出":
+  the router-gradient rewrite ``dL/dp_e = <W_down^T dL/dy, a_e>`` and
+  ``dL/da_e = p_e W_down^T dL/dy``.
+
+This module only compiles that file with gcc, loads it with ctypes and
+marshals numpy arrays. Pins (closed forms, limits, finite differences,
+brute-force tiny expert, the page's own code under autograd) live in
+``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "situ_glu_oracle.c")
+_LIB = os.path.join(_HERE, "liboracle_situ_glu.so")
+_lock = threading.Lock()
+_lib = None
+
+# The same flags on x86_64 and aarch64: no FMA contraction, no fast-math, so
+# both machines evaluate exactly the expressions written in the C file.
+GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle shared library (gcc) if missing or stale; return its path."""
+    with _lock:
+        stale = (not os.path.exists(_LIB)) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC)
+        if force or stale:
+            tmp = _LIB + f".tmp{os.getpid()}"
+            cmd = ["gcc", *GCC_FLAGS, "-o", tmp, _SRC, "-lm", "-lpthread"]
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, _LIB)
+    return _LIB
+
+
+def _load():
+    global _lib
+    if _lib is not None:
+        return _lib
+    build()
+    lib = ctypes.CDLL(_LIB)
+    i64, dbl, vp, cint = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+    lib.oracle_situ_point.argtypes = [dbl, dbl, dbl, dbl, vp]
+    lib.oracle_situ_point.restype = None
+    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+    lib.oracle_bf16_to_double.restype = dbl
+    lib.oracle_default_threads.argtypes = []
+    lib.oracle_default_threads.restype = cint
+    lib.oracle_situ_glu_fwd_f64.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
+    lib.oracle_situ_glu_fwd_f64.restype = cint
+    lib.oracle_situ_glu_bwd_router_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
+    lib.oracle_situ_glu_bwd_router_f64.restype = cint
+    lib.oracle_situ_glu_fwd_bf16.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
+    lib.oracle_situ_glu_fwd_bf16.restype = cint
+    lib.oracle_situ_glu_bwd_router_bf16.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
+    lib.oracle_situ_glu_bwd_router_bf16.restype = cint
+    _lib = lib
+    return lib
+
+
+def default_threads() -> int:
+    return int(_load().oracle_default_threads())
+
+
+def _ptr(a: np.ndarray) -> int:
+    return a.ctypes.data
+
+
+def point(u: float, v: float, beta: float = 4.0, lbeta: float = 25.0):
+    """(G, L, G', L') at one element pair, in double."""
+    res = np.zeros(4, dtype=np.float64)
+    _load().oracle_situ_point(float(u), float(v), float(beta), float(lbeta), _ptr(res))
+    return tuple(float(t) for t in res)
+
+
+def bf16_to_double(bits: int) -> float:
+    return float(_load().oracle_bf16_to_double(int(bits) & 0xFFFF))
+
+
+def _check(rc: int):
+    if rc != 0:
+        raise RuntimeError(f"oracle failed with code {rc}")
+
+
+def fwd_f64(x: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
+    """out[R,H] = G(gate)·L(linear) in double, from an fp64 x [R,2H]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    R, H2 = x.shape
+    assert H2 % 2 == 0
+    out = np.empty((R, H2 // 2), dtype=np.float64)
+    _check(_load().oracle_situ_glu_fwd_f64(_ptr(x), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
+    return out
+
+
+def bwd_router_f64(x, g, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+    """(dx [R,2H], dp [R], dp_abs [R]) in double from fp64 x [R,2H], g [R,H], p [R]."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    g = np.ascontiguousarray(g, dtype=np.float64)
+    p = np.ascontiguousarray(p, dtype=np.float64)
+    R, H2 = x.shape
+    H = H2 // 2
+    assert g.shape == (R, H) and p.shape == (R,)
+    dx = np.empty((R, H2), dtype=np.float64)
+    dp = np.empty((R,), dtype=np.float64)
+    dpa = np.empty((R,), dtype=np.float64)
+    _check(_load().oracle_situ_glu_bwd_router_f64(_ptr(x), _ptr(g), _ptr(p), _ptr(dx), _ptr(dp), _ptr(dpa),
+                                                  R, H, beta, lbeta, nthreads))
+    return dx, dp, dpa
+
+
+def fwd_bf16(x_bits: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
+    """Forward on bf16 storage bits (uint16 [R,2H]); unrounded double result [R,H]."""
+    x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+    R, H2 = x_bits.shape
+    assert H2 % 2 == 0
+    out = np.empty((R, H2 // 2), dtype=np.float64)
+    _check(_load().oracle_situ_glu_fwd_bf16(_ptr(x_bits), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
+    return out
+
+
+def bwd_router_bf16(x_bits, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+    """Backward with the router rewrite on bf16 bits x [R,2H], g [R,H] and fp32 p [R].
+
+    Returns unrounded double (dx [R,2H], dp [R], dp_abs [R]) where
+    dp_abs = Σ_j |g_j·a_j|."""
+    x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+    g_bits = np.ascontiguousarray(g_bits).view(np.uint16)
+    p = np.ascontiguousarray(p, dtype=np.float32)
+    R, H2 = x_bits.shape
+    H = H2 // 2
+    assert g_bits.shape == (R, H) and p.shape == (R,)
+    dx = np.empty((R, H2), dtype=np.float64)
+    dp = np.empty((R,), dtype=np.float64)
+    dpa = np.empty((R,), dtype=np.float64)
+    _check(_load().oracle_situ_glu_bwd_router_bf16(_ptr(x_bits), _ptr(g_bits), _ptr(p), _ptr(dx), _ptr(dp),
+                                                   _ptr(dpa), R, H, beta, lbeta, nthreads))
+    return dx, dp, dpa
