@@ -1,0 +1,463 @@
+"""Benchmark: SiTU-GLU forward + fused backward/router-gradient at the pages' scale.
+
+One step = one pass of the whole hot path over one batch of routed rows:
+    situ_glu_fwd(x) -> out        then        situ_glu_bwd_router(x, g, p) -> dx, dp
+on R = 1,600,000 rows (100k tokens x 16 experts), H = 3072, inputs resident in HBM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+Prints ONE JSON line (rank 0). ``value`` is whole-job rows/s (all ranks); the
+roofline object reports the dominant kernel (the backward) against the measured
+HBM copy bandwidth. ``--impl reference`` times the fp64 CPU oracle on the host
+cores instead (bounded sample of the same workload), for the driver's ratio.
+
+Multi-GPU: rows shard with no exchange, so each rank runs its own replica of
+the workload on its own GPU (weak scaling); only the timing is reduced (max).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "SiTU-GLU fwd+bwd rows/s and HBM GB/s (% of GB300 roofline) at R=1.6M,H=3072"
+WORKLOAD = "pages_scale_r1600000_h3072"
+FALLBACK_HBM_GBS = 6800.0
+
+# DRAM traffic of the backward kernel from one ncu capture (dram__bytes_read.sum +
+# dram__bytes_write.sum), per row, and the hash of the kernel source it was taken on.
+# Reported only while the source is unchanged; otherwise null.
+NCU_TRAFFIC = {
+    "source_sha256": None,
+    "bwd_bytes_per_row": None,
+    "fwd_bytes_per_row": None,
+    "capture": None,
+}
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for rel in ("bwd_situ_glu_gb300/csrc/situ_glu.cu", "bwd_situ_glu_gb300/csrc/situ_math.cuh"):
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--rows", type=int, default=None, help="override R (for small profiling runs)")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed plumbing
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", str(rank)))
+    return rank, world, local
+
+
+def max_over_ranks(value: float, world: int, device=None) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def whole_job_rate(units_per_rank: int, world: int, steps: int, max_seconds: float) -> float:
+    """Units all ranks processed divided by the slowest rank's time."""
+    return units_per_rank * world * steps / max_seconds
+
+
+# ---------------------------------------------------------------- peaks, clocks
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+CLOCK_FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+                "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+                "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+REASON_NAMES = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+
+
+def parse_clock_lines(lines):
+    """nvidia-smi csv,noheader,nounits lines -> {"sm_mhz", "sm_max_mhz", "reasons", "samples"}."""
+    sm, smax, reasons = [], [], set()
+    for ln in lines:
+        parts = [t.strip() for t in ln.split(",")]
+        if len(parts) < 9:
+            continue
+        try:
+            sm.append(float(parts[1]))
+            smax.append(float(parts[2]))
+        except ValueError:
+            continue
+        for name, flag in zip(REASON_NAMES, parts[5:9]):
+            if flag.lower().startswith("active"):
+                reasons.add(name)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+    return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+            "samples": len(sm)}
+
+
+class ClockSampler:
+    """Runs nvidia-smi in the background while the timed region runs."""
+
+    def __init__(self, gpu_uuid=None, period_ms=100):
+        self.cmd = ["nvidia-smi", f"--query-gpu={CLOCK_FIELDS}", "--format=csv,noheader,nounits",
+                    f"-lms", str(period_ms)]
+        if gpu_uuid:
+            self.cmd += ["-i", gpu_uuid]
+        self.lines = []
+        self.proc = None
+        self.thread = None
+        self.first = threading.Event()
+
+    def _reader(self):
+        for ln in self.proc.stdout:
+            self.lines.append(ln)
+            self.first.set()
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(self.cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._reader, daemon=True)
+        self.thread.start()
+        self.first.wait(timeout=5.0)
+        self.lines.clear()
+
+    def stop(self):
+        if self.proc is None:
+            return parse_clock_lines([])
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+        return parse_clock_lines(self.lines)
+
+
+# ---------------------------------------------------------------- CPU oracle timing
+
+def oracle_rows_per_s(x_cpu, g_cpu, p_cpu, nthreads=0):
+    """Time the fp64 oracle on one block of rows (fwd then bwd+router), return (rows/s, seconds)."""
+    import numpy as np
+    import torch
+
+    import oracle
+    xb = x_cpu.view(torch.int16).numpy().view(np.uint16)
+    gb = g_cpu.view(torch.int16).numpy().view(np.uint16)
+    pn = p_cpu.numpy()
+    t0 = time.perf_counter()
+    oracle.fwd_bf16(xb, nthreads=nthreads)
+    oracle.bwd_router_bf16(xb, gb, pn, nthreads=nthreads)
+    dt = time.perf_counter() - t0
+    return x_cpu.shape[0] / dt, dt
+
+
+def cpu_baseline(get_rows, R, target_s):
+    """Oracle rows/s on a bounded prefix of the workload, sized to ~target_s of CPU time."""
+    import oracle
+    cores = oracle.default_threads()
+    n0 = min(R, 1024)
+    x, g, p = get_rows(n0)
+    rate0, dt0 = oracle_rows_per_s(x, g, p)
+    n = int(min(R, max(n0, rate0 * target_s)))
+    n -= n % 16
+    n = max(n, 16)
+    x, g, p = get_rows(n)
+    rate, dt = oracle_rows_per_s(x, g, p)
+    return {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
+            "sample": f"first {n} of {R} rows (fwd then bwd+router grad, fp64, {cores} threads), {dt:.1f} s"}
+
+
+# ---------------------------------------------------------------- reference arm
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import situ_inputs as si
+    w = si.get(WORKLOAD)
+    R = args.rows or w.R
+    import oracle
+    oracle.build()
+    cores = oracle.default_threads()
+
+    # each step: a bounded sample of the same workload (same distributions and seed), on the host
+    def sample(n):
+        ws = si.Workload(w.name, n, w.H, w.x_kind, w.x_std, w.g_std, w.p_kind, w.order, w.seed)
+        return si.generate(ws, device="cpu")
+
+    x, g, p = sample(512)
+    rate0, _ = oracle_rows_per_s(x, g, p)
+    budget_steps = max(1, args.steps + args.warmup)
+    n = int(max(256, min(R, rate0 * 150.0 / budget_steps)))   # whole run ~ 2.5 minutes at most
+    n -= n % 16
+    x, g, p = sample(n)
+    for _ in range(args.warmup):
+        oracle_rows_per_s(x, g, p)
+    total = 0.0
+    for _ in range(args.steps):
+        _, dt = oracle_rows_per_s(x, g, p)
+        total += dt
+    rate = n * args.steps / total
+    line = {
+        "impl": "reference", "metric": METRIC, "value": rate, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "R": R, "H": w.H, "beta": 4.0, "lbeta": 25.0,
+                   "step_sample_rows": n},
+        "cpu_baseline": {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} rows of the workload per step (fwd then bwd+router grad, fp64)"},
+        "e2e": {"value": rate, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- native arm
+
+def run_native(args):
+    import torch
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+
+    import bwd_situ_glu_gb300 as sg
+    import situ_inputs as si
+    sg.build()
+    sg.load()
+
+    w = si.get(WORKLOAD)
+    R = args.rows or w.R
+    H = w.H
+    # each rank draws its own shard of routed rows (different seed per rank)
+    ws = si.Workload(w.name, R, H, w.x_kind, w.x_std, w.g_std, w.p_kind, w.order, w.seed + 1000 * rank)
+    x, g, p = si.generate(ws, device=dev)
+    out = torch.empty((R, H), dtype=torch.bfloat16, device=dev)
+    dx = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=dev)
+    dp = torch.empty((R,), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    sh = int(stream.cuda_stream)
+
+    def step():
+        sg.situ_glu_fwd_ptr(x.data_ptr(), out.data_ptr(), R, H, 4.0, 25.0, sh)
+        sg.situ_glu_bwd_router_ptr(x.data_ptr(), g.data_ptr(), p.data_ptr(), dx.data_ptr(), dp.data_ptr(),
+                                   R, H, 4.0, 25.0, sh)
+
+    torch.cuda.synchronize(dev)
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        uuid = u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    sampler.start()
+    start.record(stream)
+    for i in range(K):
+        ev[i][0].record(stream)
+        sg.situ_glu_fwd_ptr(x.data_ptr(), out.data_ptr(), R, H, 4.0, 25.0, sh)
+        ev[i][1].record(stream)
+        sg.situ_glu_bwd_router_ptr(x.data_ptr(), g.data_ptr(), p.data_ptr(), dx.data_ptr(), dp.data_ptr(),
+                                   R, H, 4.0, 25.0, sh)
+        ev[i][2].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks = sampler.stop()
+    barrier(world)
+    elapsed_ms = start.elapsed_time(end)
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    bwd_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    max_ms = max_over_ranks(elapsed_ms, world, dev)
+
+    fwd_bytes = 6 * H * R
+    bwd_bytes = (10 * H + 8) * R
+    peak, peak_src = load_peaks()
+    fwd_avg, bwd_avg = sum(fwd_ms) / K, sum(bwd_ms) / K
+    fwd_gbs = fwd_bytes / (fwd_avg * 1e-3) / 1e9
+    bwd_gbs = bwd_bytes / (bwd_avg * 1e-3) / 1e9
+    step_gbs = (fwd_bytes + bwd_bytes) / (elapsed_ms / K * 1e-3) / 1e9
+
+    traffic = None
+    if NCU_TRAFFIC["source_sha256"] == kernel_source_hash() and NCU_TRAFFIC["bwd_bytes_per_row"]:
+        traffic = NCU_TRAFFIC["bwd_bytes_per_row"] * R
+
+    # ---------------- end to end through the public API: pinned host in, pinned host out
+    e2e = None
+    if not args.no_e2e:
+        e2e = time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, args.e2e_steps, world)
+
+    # ---------------- CPU baseline: the oracle on a bounded sample (rank 0 at N = 1 only)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        def rows(n):
+            return x[:n].cpu(), g[:n].cpu(), p[:n].cpu()
+        cpu = cpu_baseline(rows, R, args.cpu_seconds)
+
+    if rank != 0:
+        return 0
+    line = {
+        "metric": METRIC,
+        "value": whole_job_rate(R, world, K, max_ms * 1e-3),
+        "unit": "rows/s",
+        "n_gpus": world,
+        "steps": K,
+        "warmup": args.warmup,
+        "ms_per_step": max_ms / K,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "R": R, "H": H, "io_dtype": "bf16", "beta": 4.0, "lbeta": 25.0,
+                   "parallelism": f"replicas x{world} (rows shard, no collective)",
+                   "l2": "inputs larger than L2 (x alone is %.2f GB vs 129 MB L2); no flush" % (4 * H * R / 1e9)},
+        "passes": {
+            "fwd": {"ms": fwd_avg, "GB_s": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
+                    "rows_per_s": R / (fwd_avg * 1e-3), "bytes": fwd_bytes},
+            "bwd_router": {"ms": bwd_avg, "GB_s": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
+                           "rows_per_s": R / (bwd_avg * 1e-3), "bytes": bwd_bytes},
+            "step_GB_s": step_gbs,
+        },
+        "roofline": {"bound": "hbm", "kernel": "bwd_vec_kernel (situ_glu_bwd_router)",
+                     "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
+                     "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
+                     if peak_src == "measured" else "fallback 6.8 TB/s",
+                     "algorithmic_bytes_per_launch": bwd_bytes, "traffic": traffic},
+        "clocks": clocks,
+        "gpu_launches": 2 * K,
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def pinned_like(t):
+    """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size)."""
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype)
+    rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 0)
+    if int(rc) != 0:
+        raise RuntimeError(f"cudaHostRegister failed: {rc}")
+    return h
+
+
+def unpin(h):
+    import torch
+    torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
+
+
+def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world):
+    """Same step through the public binding with inputs copied in from pinned host memory and
+    every result copied back, inside the timed region."""
+    import torch
+    steps = max(1, steps)
+    xh, gh, ph, oh, dxh, dph = (pinned_like(t) for t in (x, g, p, out, dx, dp))
+    xh.copy_(x)
+    gh.copy_(g)
+    ph.copy_(p)
+    h2d = xh.numel() * 2 + gh.numel() * 2 + ph.numel() * 4
+    d2h = oh.numel() * 2 + dxh.numel() * 2 + dph.numel() * 4
+
+    def one():
+        with torch.cuda.stream(stream):
+            x.copy_(xh, non_blocking=True)
+            g.copy_(gh, non_blocking=True)
+            p.copy_(ph, non_blocking=True)
+            sg.situ_glu_fwd(x, out, stream=stream)
+            sg.situ_glu_bwd_router(x, g, p, dx, dp, stream=stream)
+            oh.copy_(out, non_blocking=True)
+            dxh.copy_(dx, non_blocking=True)
+            dph.copy_(dp, non_blocking=True)
+
+    one()
+    torch.cuda.synchronize(dev)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end), world, dev)
+    for t in (xh, gh, ph, oh, dxh, dph):
+        unpin(t)
+    return {"value": whole_job_rate(R, world, steps, ms * 1e-3), "unit": "rows/s", "steps": steps,
+            "ms_per_step": ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "how": "pinned host x,g,p -> device, fwd + bwd via the binding, out,dx,dp -> pinned host; one stream"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,191 @@
+"""bwd_situ_glu_gb300 — SiTU-GLU forward and fused backward + router gradient on GB300.
+
+Thin Python binding over the C ABI in ``include/situ_glu.h`` (``libsitu_glu.so``,
+built in-tree from ``csrc/`` for sm_103a). Every step of the computation runs in
+the library's CUDA kernels; this module only checks tensor metadata, marshals
+pointers and raises on a non-zero status. There is no CPU fallback: if the
+library is missing or cannot load, every call raises.
+
+Binding names match the C entry points:
+
+* ``situ_glu_fwd(x, out=None, beta=4.0, lbeta=25.0, stream=None) -> out``
+* ``situ_glu_bwd_router(x, g, p, dx=None, dp=None, beta=4.0, lbeta=25.0, stream=None) -> (dx, dp)``
+
+Shapes: ``x`` bf16 [R, 2H] (gate | linear), ``g`` bf16 [R, H], ``p`` fp32 [R];
+``out`` bf16 [R, H], ``dx`` bf16 [R, 2H], ``dp`` fp32 [R]. All on one CUDA device.
+``dx`` may be ``x`` itself (in-place backward).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_ROOT = os.path.dirname(_HERE)
+CSRC = os.path.join(_HERE, "csrc")
+INCLUDE = os.path.join(_ROOT, "include")
+LIB_DIR = os.path.join(_HERE, "_lib")
+LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
+SOURCES = [os.path.join(CSRC, "situ_glu.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, "situ_math.cuh"), os.path.join(INCLUDE, "situ_glu.h")]
+
+NVCC_FLAGS = [
+    "-std=c++17", "-O3", "-lineinfo",
+    "-gencode", "arch=compute_103a,code=sm_103a",
+    "-Xcompiler", "-fPIC", "-shared",
+]
+
+STATUS_OK, STATUS_INVALID_ARG, STATUS_OVERLAP, STATUS_CUDA_ERROR = 0, 1, 2, 3
+
+_lock = threading.Lock()
+_lib = None
+
+
+class SituGluError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"situ_glu status {status}: {msg}")
+        self.status = status
+
+
+def _nvcc() -> str:
+    home = os.environ.get("CUDA_HOME", "/usr/local/cuda")
+    cand = os.path.join(home, "bin", "nvcc")
+    return cand if os.path.exists(cand) else "nvcc"
+
+
+def build(force: bool = False, verbose: bool = False) -> str:
+    """Compile ``libsitu_glu.so`` in-tree for sm_103a if missing or older than its sources."""
+    with _lock:
+        os.makedirs(LIB_DIR, exist_ok=True)
+        newest = max(os.path.getmtime(p) for p in DEPENDS)
+        if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
+            tmp = LIB_PATH + f".tmp{os.getpid()}"
+            cmd = [_nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, *SOURCES]
+            if verbose:
+                cmd.insert(1, "-Xptxas=-v")
+            subprocess.run(cmd, check=True)
+            os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+def load():
+    """Load the CUDA library (does not compile). Raises if it is not built."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run bwd_situ_glu_gb300.build())")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i64, f32, cint = ctypes.c_void_p, ctypes.c_int64, ctypes.c_float, ctypes.c_int
+    lib.situ_glu_fwd.argtypes = [vp, vp, i64, i64, f32, f32, vp]
+    lib.situ_glu_fwd.restype = cint
+    lib.situ_glu_bwd_router.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, f32, vp]
+    lib.situ_glu_bwd_router.restype = cint
+    lib.situ_glu_status_string.argtypes = [cint]
+    lib.situ_glu_status_string.restype = ctypes.c_char_p
+    lib.situ_glu_last_cuda_error.argtypes = []
+    lib.situ_glu_last_cuda_error.restype = cint
+    lib.situ_glu_version.argtypes = []
+    lib.situ_glu_version.restype = cint
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().situ_glu_status_string(int(status)).decode()
+
+
+def version() -> int:
+    return int(load().situ_glu_version())
+
+
+def _check(status: int):
+    if status != STATUS_OK:
+        msg = status_string(status)
+        if status == STATUS_CUDA_ERROR:
+            msg += f" (cudaError {load().situ_glu_last_cuda_error()})"
+        raise SituGluError(status, msg)
+
+
+# ---------------- raw pointer calls (ints are device addresses) ----------------
+
+def situ_glu_fwd_ptr(x: int, out: int, R: int, H: int, beta: float = 4.0, lbeta: float = 25.0,
+                     stream: int = 0) -> None:
+    _check(load().situ_glu_fwd(x, out, R, H, beta, lbeta, stream))
+
+
+def situ_glu_bwd_router_ptr(x: int, g: int, p: int, dx: int, dp: int, R: int, H: int, beta: float = 4.0,
+                            lbeta: float = 25.0, stream: int = 0) -> None:
+    _check(load().situ_glu_bwd_router(x, g, p, dx, dp, R, H, beta, lbeta, stream))
+
+
+# ---------------- torch tensor calls ----------------
+
+def _need(t, dtype, shape, name):
+    import torch
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _stream_handle(stream, device) -> int:
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def situ_glu_fwd(x, out=None, beta: float = 4.0, lbeta: float = 25.0, stream=None):
+    """out[R,H] (bf16) = SiTU-GLU(x[R,2H] bf16). Enqueued on ``stream`` (default: current)."""
+    import torch
+    if x.dim() != 2 or x.shape[1] % 2 != 0:
+        raise ValueError("x must be [R, 2H]")
+    R, H = x.shape[0], x.shape[1] // 2
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    if out is None:
+        out = torch.empty((R, H), dtype=torch.bfloat16, device=x.device)
+    _need(out, torch.bfloat16, (R, H), "out")
+    if out.device != x.device:
+        raise ValueError("x and out must be on the same device")
+    with torch.cuda.device(x.device):
+        situ_glu_fwd_ptr(x.data_ptr(), out.data_ptr(), R, H, beta, lbeta, _stream_handle(stream, x.device))
+    return out
+
+
+def situ_glu_bwd_router(x, g, p, dx=None, dp=None, beta: float = 4.0, lbeta: float = 25.0, stream=None):
+    """(dx[R,2H] bf16, dp[R] fp32) of the fused backward + router gradient. ``dx`` may be ``x``."""
+    import torch
+    if x.dim() != 2 or x.shape[1] % 2 != 0:
+        raise ValueError("x must be [R, 2H]")
+    R, H = x.shape[0], x.shape[1] // 2
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    _need(g, torch.bfloat16, (R, H), "g")
+    _need(p, torch.float32, (R,), "p")
+    if dx is None:
+        dx = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=x.device)
+    if dp is None:
+        dp = torch.empty((R,), dtype=torch.float32, device=x.device)
+    _need(dx, torch.bfloat16, (R, 2 * H), "dx")
+    _need(dp, torch.float32, (R,), "dp")
+    if len({t.device for t in (x, g, p, dx, dp)}) != 1:
+        raise ValueError("all tensors must be on the same device")
+    with torch.cuda.device(x.device):
+        situ_glu_bwd_router_ptr(x.data_ptr(), g.data_ptr(), p.data_ptr(), dx.data_ptr(), dp.data_ptr(), R, H,
+                                beta, lbeta, _stream_handle(stream, x.device))
+    return dx, dp
+
+
+__all__ = [
+    "build", "load", "version", "status_string", "SituGluError",
+    "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
+    "LIB_PATH", "INCLUDE",
+]

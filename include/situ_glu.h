@@ -1,0 +1,130 @@
+/*
+ * situ_glu.h — C ABI of the GB300 (sm_103a) SiTU-GLU library.
+ *
+ * Two operations, each one hand-written CUDA kernel launch:
+ *
+ *   situ_glu_fwd         the SiTU-GLU expert activation over routed rows.
+ *                        Defined in "Frontier-scale RL with Kimi K3", section
+ *                        "Streaming activations" (the naive situ_and_mul listing):
+ *                        split each row of x into gate | linear halves and return
+ *                        out = [beta·tanh(gate/beta)·sigmoid(gate)] · [lbeta·tanh(linear/lbeta)],
+ *                        computed in fp32 from bf16 x and rounded to bf16.
+ *
+ *   situ_glu_bwd_router  its backward, which keeps only bf16 x and recomputes
+ *                        tanh / sigmoid (same section: the custom operator,
+ *                        points 1 and 2), fused with the router-probability
+ *                        gradient of "Kimi K3 模型结构（9）：显存", section
+ *                        "MoE 反向：推一下为什么可以不存 expert 输出":
+ *                        with g = W_downᵀ·dL/dy for a routed row and that row's
+ *                        router weight p,
+ *                            dp[r]     = Σ_j g[r,j]·a[r,j]         (= dL/dp_e, no stored o_e)
+ *                            dx[r,j]   = p[r]·g[r,j]·L·G'          (gate half)
+ *                            dx[r,H+j] = p[r]·g[r,j]·G·L'          (linear half)
+ *                        where G = beta·tanh(u/beta)·sigmoid(u), L = lbeta·tanh(v/lbeta),
+ *                        G' = dG/du, L' = dL/dv, a = G·L, u = x[r,j], v = x[r,H+j].
+ *
+ * Layouts (all row-major, contiguous, little-endian):
+ *   x    bf16 [R, 2H]   gate in columns 0..H-1, linear in columns H..2H-1
+ *   out  bf16 [R, H]
+ *   g    bf16 [R, H]    NOT pre-scaled by p
+ *   p    fp32 [R]
+ *   dx   bf16 [R, 2H]   d/dgate in columns 0..H-1, d/dlinear in H..2H-1
+ *   dp   fp32 [R]
+ * bf16 tensors are passed as raw 16-bit storage (the bits of __nv_bfloat16).
+ *
+ * Arithmetic: fp32 in registers; the dp reduction uses the unrounded fp32 a,
+ * summed per row in a fixed order (results are bit-reproducible run to run).
+ * bf16 results are rounded to nearest even.
+ *
+ * Pointers are DEVICE pointers on the calling thread's current CUDA device.
+ * The caller owns every buffer. The library allocates no memory, keeps no
+ * workspace and no state beyond per-device launch-configuration caches.
+ * Calls are asynchronous on `stream` (0 = the legacy default stream) and never
+ * synchronise the host.
+ *
+ * Fast path: base pointers of x/out (fwd) or x/g/dx (bwd) 16-byte aligned and
+ * H % 8 == 0 -> 16-byte vector loads and stores. Anything else still works on a
+ * per-element path (slower). Non-finite inputs propagate (NaN in, NaN out);
+ * finite inputs of any magnitude give finite results.
+ *
+ * Return value of every compute entry point: a situ_glu_status. All argument
+ * checks happen before any CUDA call; on a non-zero status nothing was enqueued.
+ */
+#ifndef SITU_GLU_H
+#define SITU_GLU_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SITU_GLU_VERSION_MAJOR 1
+#define SITU_GLU_VERSION_MINOR 0
+#define SITU_GLU_VERSION_PATCH 0
+
+/* Largest H accepted (columns per half). */
+#define SITU_GLU_MAX_H (1LL << 30)
+
+typedef enum situ_glu_status {
+    SITU_GLU_OK = 0,
+    /* a required pointer is NULL while R > 0; R < 0; H <= 0 or H > SITU_GLU_MAX_H;
+       beta or lbeta not finite or <= 0; R*2H*2 bytes overflows int64; a bf16
+       pointer not 2-byte aligned or an fp32 pointer not 4-byte aligned */
+    SITU_GLU_INVALID_ARG = 1,
+    /* an output byte range overlaps an input or another output. The single
+       exception: situ_glu_bwd_router accepts dx == x exactly (in place). */
+    SITU_GLU_OVERLAP = 2,
+    /* a CUDA runtime call or the kernel launch failed; see situ_glu_last_cuda_error() */
+    SITU_GLU_CUDA_ERROR = 3
+} situ_glu_status;
+
+/*
+ * Forward: out[r,j] = bf16( G(x[r,j]) · L(x[r,H+j]) ) for r < R, j < H.
+ *   x      device, bf16 [R,2H], read only
+ *   out    device, bf16 [R,H], written; must not overlap x
+ *   R      rows (>= 0; R == 0 is a successful no-op, pointers may then be NULL)
+ *   H      columns per half (1 .. SITU_GLU_MAX_H)
+ *   beta   gate scale β (finite, > 0; 4 in the pages). β == 4 with λ <= 64 takes a
+ *          faster kernel that shares one exponential between tanh(u/4) and sigmoid(u)
+ *   lbeta  linear scale λ (finite, > 0; 25 in the pages)
+ *   stream CUDA stream to enqueue on
+ * Source: "Frontier-scale RL with Kimi K3", section "Streaming activations".
+ */
+int situ_glu_fwd(const void* x, void* out, int64_t R, int64_t H, float beta, float lbeta,
+                 cudaStream_t stream);
+
+/*
+ * Fused backward + router gradient (see the file comment for the formulas).
+ *   x      device, bf16 [R,2H], read only (the only tensor saved from forward)
+ *   g      device, bf16 [R,H], read only: g = W_downᵀ·dL/dy per routed row
+ *   p      device, fp32 [R], read only: router weight of each row
+ *   dx     device, bf16 [R,2H], written. May be exactly x (in place: each
+ *          element of x is read before the same thread overwrites it);
+ *          must not otherwise overlap x, g, p or dp
+ *   dp     device, fp32 [R], written; must not overlap any other buffer
+ *   R, H, beta, lbeta, stream as for situ_glu_fwd
+ * Sources: "Frontier-scale RL with Kimi K3", section "Streaming activations"
+ * (backward keeps only x and recomputes tanh and sigmoid); "Kimi K3 模型结构（9）：显存",
+ * section "MoE 反向：推一下为什么可以不存 expert 输出" (dL/dp_e = <W_downᵀ dL/dy, a_e>,
+ * dL/da_e = p_e·W_downᵀ dL/dy).
+ */
+int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, float* dp,
+                        int64_t R, int64_t H, float beta, float lbeta, cudaStream_t stream);
+
+/* Static, NUL-terminated description of a status code (unknown codes included). */
+const char* situ_glu_status_string(int status);
+
+/* The cudaError_t behind the last SITU_GLU_CUDA_ERROR returned on this host thread
+   (cudaSuccess if none). */
+int situ_glu_last_cuda_error(void);
+
+/* MAJOR*10000 + MINOR*100 + PATCH */
+int situ_glu_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SITU_GLU_H */

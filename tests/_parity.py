@@ -1,0 +1,147 @@
+"""Element-by-element comparison of the CUDA path with the fp64 oracle.
+
+Acceptance (the stated tolerance of the method's port):
+* bf16 outputs (out, dx):  |gpu - ref| <= max(ulp_bf16(ref), 1e-3),
+  ulp_bf16(ref) = 2^(floor(log2|ref|) - 7)  (0 for ref == 0, leaving the 1e-3 floor);
+* fp32 dp:  |gpu - ref| <= 1e-3·|ref| + 1e-6·Σ_j|g_j·a_j|.
+  The second term only matters where the row sum cancels to nearly zero, where a
+  purely relative bound is ill-posed; the count of rows that needed it is reported.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+import torch
+
+import oracle
+
+BF16_ABS_FLOOR = 1e-3
+DP_REL = 1e-3
+DP_ABS_SCALE = 1e-6
+
+
+def bits_of(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor (any device) -> uint16 numpy array of its storage bits."""
+    return t.detach().contiguous().cpu().view(torch.int16).numpy().view(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    mag = np.abs(ref)
+    _, e = np.frexp(mag)                 # mag = m·2^e, m in [0.5, 1)  ->  floor(log2 mag) = e - 1
+    u = np.ldexp(1.0, (e - 8).astype(np.int32))
+    return np.where(mag == 0, 0.0, u)
+
+
+@dataclass
+class Tally:
+    n: int = 0
+    bad: int = 0
+    worst_ratio: float = 0.0     # max |err| / tol
+    worst_abs: float = 0.0
+    examples: list = field(default_factory=list)
+
+
+@dataclass
+class DpTally(Tally):
+    floor_rows: int = 0          # rows that passed only thanks to the cancellation term
+    worst_rel: float = 0.0
+
+
+class Parity:
+    def __init__(self, name: str):
+        self.name = name
+        self.t = {"out": Tally(), "dx": Tally(), "dp": DpTally()}
+
+    def bf16(self, key: str, gpu_bits: np.ndarray, ref: np.ndarray, row0: int = 0):
+        gpu = bf16_bits_to_f64(gpu_bits)
+        nan_ref, nan_gpu = np.isnan(ref), np.isnan(gpu)
+        tol = np.maximum(ulp_bf16(ref), BF16_ABS_FLOOR)
+        with np.errstate(invalid="ignore"):
+            err = np.abs(gpu - ref)
+            bad = (err > tol) | (nan_ref != nan_gpu)
+            bad &= ~(nan_ref & nan_gpu)
+            ratio = np.where(nan_ref | nan_gpu, 0.0, err / tol)
+        tl = self.t[key]
+        tl.n += ref.size
+        nb = int(bad.sum())
+        tl.bad += nb
+        if ref.size:
+            tl.worst_ratio = max(tl.worst_ratio, float(np.nanmax(ratio)))
+            tl.worst_abs = max(tl.worst_abs, float(np.nanmax(np.where(nan_ref | nan_gpu, 0.0, err))))
+        if nb and len(tl.examples) < 5:
+            for idx in np.argwhere(bad)[:5 - len(tl.examples)]:
+                idx = tuple(int(i) for i in idx)
+                tl.examples.append((row0 + idx[0],) + idx[1:] + (float(gpu[idx]), float(ref[idx])))
+
+    def dp(self, gpu: np.ndarray, ref: np.ndarray, ref_abs: np.ndarray, row0: int = 0):
+        gpu = gpu.astype(np.float64)
+        err = np.abs(gpu - ref)
+        rel_tol = DP_REL * np.abs(ref)
+        tol = rel_tol + DP_ABS_SCALE * ref_abs
+        bad = ~(err <= tol)
+        tl = self.t["dp"]
+        tl.n += ref.size
+        tl.bad += int(bad.sum())
+        tl.floor_rows += int(((err > rel_tol) & ~bad).sum())
+        if ref.size:
+            tl.worst_ratio = max(tl.worst_ratio, float(np.max(np.where(tol > 0, err / np.maximum(tol, 1e-300), 0))))
+            tl.worst_abs = max(tl.worst_abs, float(err.max()))
+            nz = np.abs(ref) > 0
+            if nz.any():
+                tl.worst_rel = max(tl.worst_rel, float((err[nz] / np.abs(ref[nz])).max()))
+        for i in np.nonzero(bad)[0][:5 - len(tl.examples)]:
+            tl.examples.append((row0 + int(i), float(gpu[i]), float(ref[i]), float(ref_abs[i])))
+
+    def summary(self) -> str:
+        parts = [self.name]
+        for k, tl in self.t.items():
+            if tl.n:
+                s = f"{k}: n={tl.n} bad={tl.bad} worst_err/tol={tl.worst_ratio:.3g} max_abs={tl.worst_abs:.3g}"
+                if k == "dp":
+                    s += f" max_rel={tl.worst_rel:.3g} floor_rows={tl.floor_rows}"
+                parts.append(s)
+        return " | ".join(parts)
+
+    def assert_ok(self):
+        print(self.summary())
+        for k, tl in self.t.items():
+            assert tl.bad == 0, f"{self.name}: {k} has {tl.bad} elements out of tolerance, e.g. {tl.examples}"
+
+
+def compare_rows(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, row0=0, nthreads=0):
+    """Compare one block of rows (CPU or GPU tensors) against the oracle. Any of out / dx+dp may be None."""
+    xb = bits_of(x)
+    if out is not None:
+        ref = oracle.fwd_bf16(xb, beta, lbeta, nthreads)
+        par.bf16("out", bits_of(out), ref, row0)
+    if dx is not None:
+        dx_ref, dp_ref, dpa = oracle.bwd_router_bf16(xb, bits_of(g), p.detach().cpu().numpy(), beta, lbeta, nthreads)
+        par.bf16("dx", bits_of(dx), dx_ref, row0)
+        par.dp(dp.detach().cpu().numpy(), dp_ref, dpa, row0)
+
+
+def compare_full(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, chunk_rows=8192):
+    R = x.shape[0]
+    for r0 in range(0, R, chunk_rows):
+        r1 = min(R, r0 + chunk_rows)
+        compare_rows(par, x[r0:r1], None if g is None else g[r0:r1], None if p is None else p[r0:r1],
+                     None if out is None else out[r0:r1], None if dx is None else dx[r0:r1],
+                     None if dp is None else dp[r0:r1], beta, lbeta, row0=r0)
+
+
+def sample_rows(R: int, n_random: int = 2048, edge: int = 64, seed: int = 0) -> torch.Tensor:
+    rng = np.random.default_rng(seed)
+    idx = set(range(min(edge, R))) | set(range(max(0, R - edge), R))
+    idx |= set(rng.integers(0, R, size=min(n_random, R)).tolist())
+    return torch.tensor(sorted(idx), dtype=torch.int64)
+
+
+def compare_sampled(par: Parity, x, g, p, out, dx, dp, rows: torch.Tensor, beta=4.0, lbeta=25.0):
+    dev_rows = rows.to(x.device)
+    take = lambda t: None if t is None else t.index_select(0, dev_rows)
+    compare_rows(par, take(x), take(g), take(p), take(out), take(dx), take(dp), beta, lbeta)

@@ -1,0 +1,133 @@
+"""The C ABI library loads, exports every function include/*.h declares, and rejects bad
+arguments on the host before any CUDA call.
+
+No test here launches a kernel: every call below fails validation first, so the
+pointers are plain integers that are never dereferenced. (A fully valid set of
+fake pointers would reach a launch; none is ever passed.)
+"""
+import glob
+import os
+import re
+
+import pytest
+
+import bwd_situ_glu_gb300 as sg
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+OK, INVALID, OVERLAP = 0, 1, 2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    sg.build()
+    return sg.load()
+
+
+def _declared_functions():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        text = open(h).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*[A-Za-z_][\w\s\*]*?\b(situ_glu_\w+)\s*\(", text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = _declared_functions()
+    for n in ("situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_status_string", "situ_glu_version",
+              "situ_glu_last_cuda_error"):
+        assert n in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    missing = [n for n in _declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_version_and_status_strings(lib):
+    assert sg.version() == 10000
+    for s in (0, 1, 2, 3, 99, -1):
+        assert isinstance(sg.status_string(s), str) and sg.status_string(s)
+    assert sg.status_string(0) == "ok"
+    assert lib.situ_glu_last_cuda_error() == 0
+
+
+A = 1 << 20  # fake, 16-byte aligned "device" addresses: never dereferenced
+B = 1 << 40
+
+
+def fwd(lib, x, out, R, H, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_fwd(x, out, R, H, beta, lbeta, None)
+
+
+def bwd(lib, x, g, p, dx, dp, R, H, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_bwd_router(x, g, p, dx, dp, R, H, beta, lbeta, None)
+
+
+def test_empty_is_a_noop(lib):
+    assert fwd(lib, None, None, 0, 3072) == OK
+    assert bwd(lib, None, None, None, None, None, 0, 3072) == OK
+
+
+@pytest.mark.parametrize("R,H", [(-1, 8), (4, 0), (4, -8), (4, (1 << 30) + 1), (1 << 62, 3072)])
+def test_bad_shapes(lib, R, H):
+    assert fwd(lib, A, B, R, H) == INVALID
+    assert bwd(lib, A, A + (1 << 36), A + (2 << 36), B, B + (1 << 36), R, H) == INVALID
+
+
+@pytest.mark.parametrize("beta,lbeta", [(0.0, 25.0), (-4.0, 25.0), (4.0, 0.0), (float("nan"), 25.0),
+                                        (4.0, float("inf")), (float("inf"), 25.0)])
+def test_bad_scales(lib, beta, lbeta):
+    assert fwd(lib, A, B, 4, 8, beta, lbeta) == INVALID
+    assert bwd(lib, A, A + 4096, A + 8192, B, B + 4096, 4, 8, beta, lbeta) == INVALID
+
+
+def test_null_pointers(lib):
+    assert fwd(lib, None, B, 4, 8) == INVALID
+    assert fwd(lib, A, None, 4, 8) == INVALID
+    args = [A, A + 4096, A + 8192, B, B + 4096]
+    for i in range(5):
+        a = list(args)
+        a[i] = None
+        assert bwd(lib, *a, 4, 8) == INVALID
+
+
+def test_misaligned_pointers(lib):
+    assert fwd(lib, A + 1, B, 4, 8) == INVALID               # bf16 needs 2-byte alignment
+    assert fwd(lib, A, B + 1, 4, 8) == INVALID
+    assert bwd(lib, A, A + 4096, A + 8192 + 2, B, B + 4096, 4, 8) == INVALID   # p needs 4 bytes
+    assert bwd(lib, A, A + 4096, A + 8192, B, B + 4096 + 2, 4, 8) == INVALID   # dp needs 4 bytes
+    assert bwd(lib, A, A + 4096 + 1, A + 8192, B, B + 4096, 4, 8) == INVALID   # g
+
+
+def test_forward_overlap(lib):
+    R, H = 4, 8                      # x: 128 B, out: 64 B
+    assert fwd(lib, A, A, R, H) == OVERLAP
+    assert fwd(lib, A, A + 126, R, H) == OVERLAP
+    assert fwd(lib, A + 62, A, R, H) == OVERLAP
+
+
+def test_backward_overlap(lib):
+    R, H = 4, 8                      # x, dx: 128 B; g: 64 B; p, dp: 16 B
+    x, g, p = A, A + 4096, A + 8192
+    dx, dp = B, B + 4096
+    assert bwd(lib, x, g, p, x + 2, dp, R, H) == OVERLAP        # partial dx/x overlap
+    assert bwd(lib, x, g, p, g, dp, R, H) == OVERLAP            # dx over g
+    assert bwd(lib, x, g, p, p - 64, dp, R, H) == OVERLAP       # dx over p
+    assert bwd(lib, x, g, p, dx, dx + 64, R, H) == OVERLAP      # dp inside dx
+    assert bwd(lib, x, g, p, dx, x + 32, R, H) == OVERLAP       # dp over x
+    assert bwd(lib, x, g, p, dx, g, R, H) == OVERLAP            # dp over g
+    assert bwd(lib, x, g, p, dx, p, R, H) == OVERLAP            # dp over p
+    # the in-place form dx == x passes the overlap checks; it must still not overlap g / p / dp
+    assert bwd(lib, x, x + 64, p, x, dp, R, H) == OVERLAP       # g inside x == dx
+    assert bwd(lib, x, g, p, x, x + 16, R, H) == OVERLAP        # dp inside x == dx
+
+
+def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    import importlib
+    mod = importlib.import_module("bwd_situ_glu_gb300")
+    monkeypatch.setattr(mod, "_lib", None)
+    monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        mod.load()

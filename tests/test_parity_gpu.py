@@ -1,0 +1,326 @@
+"""Parity of the CUDA path (through the C ABI) with the fp64 oracle, on a GPU.
+
+Every input is seeded and synthetic (situ_inputs); the very same tensors are fed
+to both sides. Small and medium workloads are compared element by element over
+all rows; the pages' scale (R = 1.6M) and the largest tail-sweep shapes are run
+at full size, in the same launch as the benchmark, and compared on sampled rows
+plus properties that hold at any size.
+"""
+import numpy as np
+import pytest
+import torch
+
+import situ_inputs as si
+from _parity import Parity, bits_of, compare_full, compare_sampled, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def sg(cuda_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    return cuda_lib
+
+
+def run(sg, x, g, p, beta=4.0, lbeta=25.0):
+    out = sg.situ_glu_fwd(x, beta=beta, lbeta=lbeta)
+    dx, dp = sg.situ_glu_bwd_router(x, g, p, beta=beta, lbeta=lbeta)
+    torch.cuda.synchronize()
+    return out, dx, dp
+
+
+def on_device(w, gen_on_device=False):
+    if gen_on_device:
+        return si.generate(w, device=DEV)
+    return tuple(t.to(DEV) for t in si.generate(w, device="cpu"))
+
+
+def free(*ts):
+    del ts
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
+# ---------------------------------------------------------------- the workloads
+
+@pytest.mark.parametrize("name", ["routed_r1024_h3072", "saturating_mix_r16384_h3072"])
+def test_workload_all_rows(sg, name):
+    w = si.get(name)
+    x, g, p = on_device(w)
+    out, dx, dp = run(sg, x, g, p)
+    par = Parity(name)
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+
+
+@pytest.mark.slow
+def test_expert_grouped_all_rows(sg):
+    w = si.get("expert_grouped_r262144_h3072")
+    x, g, p = on_device(w, gen_on_device=True)
+    out, dx, dp = run(sg, x, g, p)
+    par = Parity(w.name)
+    compare_full(par, x, g, p, out, dx, dp, chunk_rows=16384)
+    par.assert_ok()
+    free(x, g, p, out, dx, dp)
+
+
+@pytest.mark.slow
+def test_pages_scale_full_launch_sampled_rows(sg):
+    """R = 1.6M, H = 3072 (x alone 19.66 GB): the benchmark's launch, checked on sampled rows."""
+    w = si.get("pages_scale_r1600000_h3072")
+    x, g, p = on_device(w, gen_on_device=True)
+    out, dx, dp = run(sg, x, g, p)
+    # properties at every element: finite outputs, |out| <= beta·lbeta, dp finite
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(dx).all()) and bool(torch.isfinite(dp).all())
+    assert float(out.abs().max()) <= 100.0
+    par = Parity(w.name + " (sampled)")
+    compare_sampled(par, x, g, p, out, dx, dp, sample_rows(w.R, n_random=4096, seed=3))
+    par.assert_ok()
+    free(x, g, p, out, dx, dp)
+
+
+@pytest.mark.parametrize("H", si.TAIL_SWEEP_H)
+@pytest.mark.parametrize("R", [1, 37, 65537])
+def test_tail_sweep_all_rows(sg, R, H):
+    w = si.tail_sweep(R, H)
+    x, g, p = on_device(w)
+    out, dx, dp = run(sg, x, g, p)
+    par = Parity(w.name)
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("H", si.TAIL_SWEEP_H)
+def test_tail_sweep_largest_sampled(sg, H):
+    w = si.tail_sweep(524288, H)
+    x, g, p = on_device(w, gen_on_device=True)
+    out, dx, dp = run(sg, x, g, p)
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(dx).all()) and bool(torch.isfinite(dp).all())
+    par = Parity(w.name + " (sampled)")
+    compare_sampled(par, x, g, p, out, dx, dp, sample_rows(w.R, seed=H))
+    par.assert_ok()
+    free(x, g, p, out, dx, dp)
+
+
+# ---------------------------------------------------------------- edge cases
+
+@pytest.mark.parametrize("beta,lbeta", [(4.0, 25.0), (2.5, 7.0)])
+@pytest.mark.parametrize("H", [1, 2, 7, 8, 9, 16, 999, 1000, 1016])
+def test_odd_widths(sg, H, beta, lbeta):
+    w = si.custom(37, H, seed=H, x_std=4.0)
+    x, g, p = on_device(w)
+    out, dx, dp = run(sg, x, g, p, beta, lbeta)
+    par = Parity(f"H={H} beta={beta} lbeta={lbeta}")
+    compare_full(par, x, g, p, out, dx, dp, beta, lbeta)
+    par.assert_ok()
+
+
+@pytest.mark.parametrize("beta,lbeta", [(4.0, 25.0), (1.0, 1.0), (0.5, 3.0), (4.0, 100.0), (8.0, 64.0),
+                                        (1e6, 1e6), (4.0, 1e6)])
+def test_other_scales(sg, beta, lbeta):
+    """Fast (beta = 4, lbeta <= 64) and general kernels, including the SwiGLU-like limit."""
+    w = si.custom(64, 1024, seed=7, x_std=3.0)
+    x, g, p = on_device(w)
+    out, dx, dp = run(sg, x, g, p, beta, lbeta)
+    par = Parity(f"beta={beta} lbeta={lbeta}")
+    compare_full(par, x, g, p, out, dx, dp, beta, lbeta)
+    par.assert_ok()
+
+
+@pytest.mark.parametrize("H", [3072, 1000, 8])
+def test_misaligned_bases_take_the_element_path(sg, H):
+    R = 21
+    w = si.custom(R, H, seed=5)
+    x0, g0, p0 = on_device(w)
+    # views whose base addresses are 2 bytes past a 16-byte boundary
+    xb = torch.empty(R * 2 * H + 8, dtype=torch.bfloat16, device=DEV)
+    gb = torch.empty(R * H + 8, dtype=torch.bfloat16, device=DEV)
+    ob = torch.empty(R * H + 8, dtype=torch.bfloat16, device=DEV)
+    db = torch.empty(R * 2 * H + 8, dtype=torch.bfloat16, device=DEV)
+    x = xb[1:1 + R * 2 * H].view(R, 2 * H)
+    g = gb[1:1 + R * H].view(R, H)
+    out = ob[1:1 + R * H].view(R, H)
+    dx = db[1:1 + R * 2 * H].view(R, 2 * H)
+    assert x.data_ptr() % 16 == 2
+    x.copy_(x0)
+    g.copy_(g0)
+    dp = torch.empty(R, dtype=torch.float32, device=DEV)
+    sg.situ_glu_fwd(x, out)
+    sg.situ_glu_bwd_router(x, g, p0, dx, dp)
+    torch.cuda.synchronize()
+    par = Parity(f"misaligned H={H}")
+    compare_full(par, x, g, p0, out, dx, dp)
+    par.assert_ok()
+    # and the aligned vector path gives the same bits
+    out2, dx2, dp2 = run(sg, x0, g0, p0)
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(dx.view(torch.int16), dx2.view(torch.int16))
+    assert torch.equal(dp, dp2)
+
+
+def test_extreme_and_nonfinite_inputs(sg):
+    H = 16
+    big = 3.3895313892515355e38  # largest finite bf16
+    vals = [0.0, -0.0, 1e-30, -1e-30, 1e-3, -1e-3, 80.0, -80.0, 500.0, -500.0, big, -big,
+            float("inf"), float("-inf"), 3.0, -3.0]
+    gate = torch.tensor(vals, dtype=torch.float32)
+    rows = []
+    for k in range(H):
+        lin = torch.roll(gate, k)
+        rows.append(torch.cat([gate, lin]))
+    x = torch.stack(rows).to(torch.bfloat16).to(DEV)
+    R = x.shape[0]
+    g = torch.linspace(-2, 2, R * H).reshape(R, H).to(torch.bfloat16).to(DEV)
+    p = torch.linspace(0.1, 1.0, R).to(DEV)
+    out, dx, dp = run(sg, x, g, p)
+    assert bool(torch.isfinite(out).all()) and bool(torch.isfinite(dx).all()) and bool(torch.isfinite(dp).all())
+    par = Parity("extreme")
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+    # NaN propagates to the outputs of its own element (and to dp of its row)
+    xn = x.clone()
+    xn[3, 5] = float("nan")
+    outn, dxn, dpn = run(sg, xn, g, p)
+    assert bool(torch.isnan(outn[3, 5])) and bool(torch.isnan(dxn[3, 5])) and bool(torch.isnan(dpn[3]))
+    mask = torch.ones_like(outn, dtype=torch.bool)
+    mask[3, 5] = False
+    assert torch.equal(outn[mask].view(torch.int16), out[mask].view(torch.int16))
+
+
+def test_zero_and_saturated_rows(sg):
+    """Closed forms through the GPU: G(0) = L(0) = 0, G'(0) = 1/2, L'(0) = 1, G(+inf) = 4,
+    L(-inf) = -25, G(-inf) = G'(+-inf) = L'(+-inf) = 0 (|x| = 1024 saturates every exponential)."""
+    H = 3072
+    x = torch.zeros(4, 2 * H, dtype=torch.bfloat16, device=DEV)
+    x[1, :H] = 1024.0         # gate saturated high, linear zero
+    x[2, H:] = -1024.0        # gate zero, linear saturated low
+    x[3, :H] = -1024.0        # both saturated
+    x[3, H:] = 1024.0
+    g = torch.ones(4, H, dtype=torch.bfloat16, device=DEV)
+    p = torch.full((4,), 0.5, device=DEV)
+    out, dx, dp = run(sg, x, g, p)
+    assert torch.all(out == 0) and torch.all(dp == 0)
+    assert torch.all(dx[0] == 0) and torch.all(dx[3] == 0)
+    assert torch.all(dx[1, :H] == 0) and torch.all(dx[1, H:] == 2.0)      # p·g·G(+inf)·L'(0) = 0.5·4·1
+    assert torch.all(dx[2, :H] == -6.25) and torch.all(dx[2, H:] == 0)    # p·g·L(-inf)·G'(0) = 0.5·(-25)·0.5
+    par = Parity("zero/saturated rows")
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+
+
+def test_empty_is_a_noop(sg):
+    x = torch.empty(0, 6144, dtype=torch.bfloat16, device=DEV)
+    g = torch.empty(0, 3072, dtype=torch.bfloat16, device=DEV)
+    p = torch.empty(0, dtype=torch.float32, device=DEV)
+    out, dx, dp = run(sg, x, g, p)
+    assert out.shape == (0, 3072) and dx.shape == (0, 6144) and dp.shape == (0,)
+
+
+# ---------------------------------------------------------------- behaviour of the boundary
+
+def test_in_place_backward_matches_out_of_place(sg):
+    w = si.custom(300, 3072, seed=11)
+    x, g, p = on_device(w)
+    _, dx_ref, dp_ref = run(sg, x, g, p)
+    xi = x.clone()
+    dx_i, dp_i = sg.situ_glu_bwd_router(xi, g, p, dx=xi)
+    torch.cuda.synchronize()
+    assert dx_i.data_ptr() == xi.data_ptr()
+    assert torch.equal(dx_i.view(torch.int16), dx_ref.view(torch.int16))
+    assert torch.equal(dp_i, dp_ref)
+    # element path in place as well
+    w2 = si.custom(30, 999, seed=12)
+    x2, g2, p2 = on_device(w2)
+    _, dxr, dpr = run(sg, x2, g2, p2)
+    x2i = x2.clone()
+    sg.situ_glu_bwd_router(x2i, g2, p2, dx=x2i)
+    torch.cuda.synchronize()
+    assert torch.equal(x2i.view(torch.int16), dxr.view(torch.int16))
+
+
+@pytest.mark.parametrize("R,H", [(37, 3072), (5, 1000), (3, 999)])
+def test_guard_bands_untouched(sg, R, H):
+    """Outputs sit inside larger buffers filled with a NaN pattern; nothing outside them changes."""
+    pad = 64
+    w = si.custom(R, H, seed=2)
+    x, g, p = on_device(w)
+    poison = torch.tensor(0x7FC1, dtype=torch.int16)
+    ob = torch.full((R * H + 2 * pad,), int(poison), dtype=torch.int16, device=DEV)
+    db = torch.full((R * 2 * H + 2 * pad,), int(poison), dtype=torch.int16, device=DEV)
+    pb = torch.full((R + 2 * pad,), float("nan"), dtype=torch.float32, device=DEV)
+    out = ob[pad:pad + R * H].view(torch.bfloat16).view(R, H)
+    dx = db[pad:pad + R * 2 * H].view(torch.bfloat16).view(R, 2 * H)
+    dp = pb[pad:pad + R]
+    sg.situ_glu_fwd(x, out)
+    sg.situ_glu_bwd_router(x, g, p, dx, dp)
+    torch.cuda.synchronize()
+    for buf, n in ((ob, R * H), (db, R * 2 * H)):
+        assert bool((buf[:pad] == poison).all()) and bool((buf[pad + n:] == poison).all())
+    assert bool(torch.isnan(pb[:pad]).all()) and bool(torch.isnan(pb[pad + R:]).all())
+    par = Parity(f"guarded R={R} H={H}")
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+
+
+def test_bitwise_reproducible(sg):
+    w = si.custom(2048, 3072, seed=21)
+    x, g, p = on_device(w)
+    a = run(sg, x, g, p)
+    b = run(sg, x, g, p)
+    assert torch.equal(a[0].view(torch.int16), b[0].view(torch.int16))
+    assert torch.equal(a[1].view(torch.int16), b[1].view(torch.int16))
+    assert torch.equal(a[2], b[2])
+
+
+def test_library_allocates_no_device_memory(sg):
+    w = si.custom(4096, 3072, seed=8)
+    x, g, p = on_device(w)
+    out = torch.empty(4096, 3072, dtype=torch.bfloat16, device=DEV)
+    dx = torch.empty_like(x)
+    dp = torch.empty(4096, dtype=torch.float32, device=DEV)
+    sg.situ_glu_fwd(x, out)
+    sg.situ_glu_bwd_router(x, g, p, dx, dp)
+    torch.cuda.synchronize()
+    free_before, _ = torch.cuda.mem_get_info()
+    for _ in range(5):
+        sg.situ_glu_fwd(x, out)
+        sg.situ_glu_bwd_router(x, g, p, dx, dp)
+    torch.cuda.synchronize()
+    free_after, _ = torch.cuda.mem_get_info()
+    assert free_after == free_before
+
+
+def test_runs_on_the_given_stream(sg):
+    w = si.custom(512, 3072, seed=4)
+    x, g, p = on_device(w)
+    ref = run(sg, x, g, p)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        out = sg.situ_glu_fwd(x)
+        dx, dp = sg.situ_glu_bwd_router(x, g, p)
+    s.synchronize()
+    assert torch.equal(out.view(torch.int16), ref[0].view(torch.int16))
+    assert torch.equal(dx.view(torch.int16), ref[1].view(torch.int16))
+    assert torch.equal(dp, ref[2])
+
+
+def test_binding_rejects_bad_tensors(sg):
+    x = torch.zeros(4, 16, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(TypeError):
+        sg.situ_glu_fwd(x.float())
+    with pytest.raises(ValueError):
+        sg.situ_glu_fwd(x[:, ::2])
+    with pytest.raises(sg.SituGluError) as ei:
+        sg.situ_glu_fwd(x, beta=-1.0)
+    assert ei.value.status == 1
+    # a partial overlap of dx with x is rejected before any launch
+    big = torch.zeros(8, 16, dtype=torch.bfloat16, device=DEV)
+    xo = big[0:4]
+    dxo = big[2:6]
+    with pytest.raises(sg.SituGluError) as ei:
+        sg.situ_glu_bwd_router(xo, torch.zeros(4, 8, dtype=torch.bfloat16, device=DEV),
+                               torch.zeros(4, device=DEV), dx=dxo)
+    assert ei.value.status == 2
