@@ -50,48 +50,95 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
-def _load():
-    global _lib
-    if _lib is not None:
-        return _lib
-    build()
-    lib = ctypes.CDLL(_LIB)
-    i64, dbl, vp, cint = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
-    lib.oracle_situ_point.argtypes = [dbl, dbl, dbl, dbl, vp]
-    lib.oracle_situ_point.restype = None
-    lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
-    lib.oracle_bf16_to_double.restype = dbl
-    lib.oracle_default_threads.argtypes = []
-    lib.oracle_default_threads.restype = cint
-    lib.oracle_situ_glu_fwd_f64.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
-    lib.oracle_situ_glu_fwd_f64.restype = cint
-    lib.oracle_situ_glu_bwd_router_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
-    lib.oracle_situ_glu_bwd_router_f64.restype = cint
-    lib.oracle_situ_glu_fwd_bf16.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
-    lib.oracle_situ_glu_fwd_bf16.restype = cint
-    lib.oracle_situ_glu_bwd_router_bf16.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
-    lib.oracle_situ_glu_bwd_router_bf16.restype = cint
-    _lib = lib
-    return lib
+class Oracle:
+    """ctypes wrapper over one build of the oracle library."""
 
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, dbl, vp, cint = ctypes.c_int64, ctypes.c_double, ctypes.c_void_p, ctypes.c_int
+        lib.oracle_situ_point.argtypes = [dbl, dbl, dbl, dbl, vp]
+        lib.oracle_situ_point.restype = None
+        lib.oracle_bf16_to_double.argtypes = [ctypes.c_uint16]
+        lib.oracle_bf16_to_double.restype = dbl
+        lib.oracle_default_threads.argtypes = []
+        lib.oracle_default_threads.restype = cint
+        lib.oracle_situ_glu_fwd_f64.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
+        lib.oracle_situ_glu_fwd_f64.restype = cint
+        lib.oracle_situ_glu_bwd_router_f64.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
+        lib.oracle_situ_glu_bwd_router_f64.restype = cint
+        lib.oracle_situ_glu_fwd_bf16.argtypes = [vp, vp, i64, i64, dbl, dbl, cint]
+        lib.oracle_situ_glu_fwd_bf16.restype = cint
+        lib.oracle_situ_glu_bwd_router_bf16.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
+        lib.oracle_situ_glu_bwd_router_bf16.restype = cint
+        self.lib = lib
+        self.path = path
 
-def default_threads() -> int:
-    return int(_load().oracle_default_threads())
+    def default_threads(self) -> int:
+        return int(self.lib.oracle_default_threads())
+
+    def point(self, u: float, v: float, beta: float = 4.0, lbeta: float = 25.0):
+        """(G, L, G', L') at one element pair, in double."""
+        res = np.zeros(4, dtype=np.float64)
+        self.lib.oracle_situ_point(float(u), float(v), float(beta), float(lbeta), _ptr(res))
+        return tuple(float(t) for t in res)
+
+    def bf16_to_double(self, bits: int) -> float:
+        return float(self.lib.oracle_bf16_to_double(int(bits) & 0xFFFF))
+
+    def fwd_f64(self, x: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
+        """out[R,H] = G(gate)·L(linear) in double, from an fp64 x [R,2H]."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        R, H2 = x.shape
+        assert H2 % 2 == 0
+        out = np.empty((R, H2 // 2), dtype=np.float64)
+        _check(self.lib.oracle_situ_glu_fwd_f64(_ptr(x), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
+        return out
+
+    def bwd_router_f64(self, x, g, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+        """(dx [R,2H], dp [R], dp_abs [R]) in double from fp64 x [R,2H], g [R,H], p [R]."""
+        x = np.ascontiguousarray(x, dtype=np.float64)
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        p = np.ascontiguousarray(p, dtype=np.float64)
+        R, H2 = x.shape
+        H = H2 // 2
+        assert g.shape == (R, H) and p.shape == (R,)
+        dx = np.empty((R, H2), dtype=np.float64)
+        dp = np.empty((R,), dtype=np.float64)
+        dpa = np.empty((R,), dtype=np.float64)
+        _check(self.lib.oracle_situ_glu_bwd_router_f64(_ptr(x), _ptr(g), _ptr(p), _ptr(dx), _ptr(dp), _ptr(dpa),
+                                                       R, H, beta, lbeta, nthreads))
+        return dx, dp, dpa
+
+    def fwd_bf16(self, x_bits: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
+        """Forward on bf16 storage bits (uint16 [R,2H]); unrounded double result [R,H]."""
+        x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+        R, H2 = x_bits.shape
+        assert H2 % 2 == 0
+        out = np.empty((R, H2 // 2), dtype=np.float64)
+        _check(self.lib.oracle_situ_glu_fwd_bf16(_ptr(x_bits), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
+        return out
+
+    def bwd_router_bf16(self, x_bits, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+        """Backward with the router rewrite on bf16 bits x [R,2H], g [R,H] and fp32 p [R].
+
+        Returns unrounded double (dx [R,2H], dp [R], dp_abs [R]) where
+        dp_abs = Σ_j |g_j·a_j|."""
+        x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+        g_bits = np.ascontiguousarray(g_bits).view(np.uint16)
+        p = np.ascontiguousarray(p, dtype=np.float32)
+        R, H2 = x_bits.shape
+        H = H2 // 2
+        assert g_bits.shape == (R, H) and p.shape == (R,)
+        dx = np.empty((R, H2), dtype=np.float64)
+        dp = np.empty((R,), dtype=np.float64)
+        dpa = np.empty((R,), dtype=np.float64)
+        _check(self.lib.oracle_situ_glu_bwd_router_bf16(_ptr(x_bits), _ptr(g_bits), _ptr(p), _ptr(dx), _ptr(dp),
+                                                        _ptr(dpa), R, H, beta, lbeta, nthreads))
+        return dx, dp, dpa
 
 
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
-
-
-def point(u: float, v: float, beta: float = 4.0, lbeta: float = 25.0):
-    """(G, L, G', L') at one element pair, in double."""
-    res = np.zeros(4, dtype=np.float64)
-    _load().oracle_situ_point(float(u), float(v), float(beta), float(lbeta), _ptr(res))
-    return tuple(float(t) for t in res)
-
-
-def bf16_to_double(bits: int) -> float:
-    return float(_load().oracle_bf16_to_double(int(bits) & 0xFFFF))
 
 
 def _check(rc: int):
@@ -99,56 +146,51 @@ def _check(rc: int):
         raise RuntimeError(f"oracle failed with code {rc}")
 
 
-def fwd_f64(x: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
-    """out[R,H] = G(gate)·L(linear) in double, from an fp64 x [R,2H]."""
-    x = np.ascontiguousarray(x, dtype=np.float64)
-    R, H2 = x.shape
-    assert H2 % 2 == 0
-    out = np.empty((R, H2 // 2), dtype=np.float64)
-    _check(_load().oracle_situ_glu_fwd_f64(_ptr(x), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
-    return out
+def _default() -> Oracle:
+    global _lib
+    if _lib is None:
+        build()
+        _lib = Oracle(_LIB)
+    return _lib
+
+
+def compile_variant(src_text: str, out_path: str) -> Oracle:
+    """Compile C source text with the oracle's flags into out_path and load it (used by tests)."""
+    src = out_path + ".c"
+    with open(src, "w") as f:
+        f.write(src_text)
+    subprocess.run(["gcc", *GCC_FLAGS, "-o", out_path, src, "-lm", "-lpthread"], check=True)
+    return Oracle(out_path)
+
+
+def source_text() -> str:
+    with open(_SRC) as f:
+        return f.read()
+
+
+def default_threads() -> int:
+    return _default().default_threads()
+
+
+def point(u: float, v: float, beta: float = 4.0, lbeta: float = 25.0):
+    return _default().point(u, v, beta, lbeta)
+
+
+def bf16_to_double(bits: int) -> float:
+    return _default().bf16_to_double(bits)
+
+
+def fwd_f64(x, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+    return _default().fwd_f64(x, beta, lbeta, nthreads)
 
 
 def bwd_router_f64(x, g, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
-    """(dx [R,2H], dp [R], dp_abs [R]) in double from fp64 x [R,2H], g [R,H], p [R]."""
-    x = np.ascontiguousarray(x, dtype=np.float64)
-    g = np.ascontiguousarray(g, dtype=np.float64)
-    p = np.ascontiguousarray(p, dtype=np.float64)
-    R, H2 = x.shape
-    H = H2 // 2
-    assert g.shape == (R, H) and p.shape == (R,)
-    dx = np.empty((R, H2), dtype=np.float64)
-    dp = np.empty((R,), dtype=np.float64)
-    dpa = np.empty((R,), dtype=np.float64)
-    _check(_load().oracle_situ_glu_bwd_router_f64(_ptr(x), _ptr(g), _ptr(p), _ptr(dx), _ptr(dp), _ptr(dpa),
-                                                  R, H, beta, lbeta, nthreads))
-    return dx, dp, dpa
+    return _default().bwd_router_f64(x, g, p, beta, lbeta, nthreads)
 
 
-def fwd_bf16(x_bits: np.ndarray, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0) -> np.ndarray:
-    """Forward on bf16 storage bits (uint16 [R,2H]); unrounded double result [R,H]."""
-    x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
-    R, H2 = x_bits.shape
-    assert H2 % 2 == 0
-    out = np.empty((R, H2 // 2), dtype=np.float64)
-    _check(_load().oracle_situ_glu_fwd_bf16(_ptr(x_bits), _ptr(out), R, H2 // 2, beta, lbeta, nthreads))
-    return out
+def fwd_bf16(x_bits, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+    return _default().fwd_bf16(x_bits, beta, lbeta, nthreads)
 
 
 def bwd_router_bf16(x_bits, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
-    """Backward with the router rewrite on bf16 bits x [R,2H], g [R,H] and fp32 p [R].
-
-    Returns unrounded double (dx [R,2H], dp [R], dp_abs [R]) where
-    dp_abs = Σ_j |g_j·a_j|."""
-    x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
-    g_bits = np.ascontiguousarray(g_bits).view(np.uint16)
-    p = np.ascontiguousarray(p, dtype=np.float32)
-    R, H2 = x_bits.shape
-    H = H2 // 2
-    assert g_bits.shape == (R, H) and p.shape == (R,)
-    dx = np.empty((R, H2), dtype=np.float64)
-    dp = np.empty((R,), dtype=np.float64)
-    dpa = np.empty((R,), dtype=np.float64)
-    _check(_load().oracle_situ_glu_bwd_router_bf16(_ptr(x_bits), _ptr(g_bits), _ptr(p), _ptr(dx), _ptr(dp),
-                                                   _ptr(dpa), R, H, beta, lbeta, nthreads))
-    return dx, dp, dpa
+    return _default().bwd_router_bf16(x_bits, g_bits, p, beta, lbeta, nthreads)

@@ -1,0 +1,293 @@
+"""Pins of the fp64 oracle against what the pages and the mathematics fix (shared bodies).
+
+Each pin_* takes an oracle instance (the real one, or a deliberately broken copy in
+tests/test_oracle_mutants.py) and raises AssertionError when the oracle disagrees.
+
+Nothing here runs on a GPU. Each test is chosen so that a plausible mistake in
+the oracle (a dropped term of G', a wrong sign in the overflow-safe sigmoid, a
+swapped gate/linear half, p folded into dp, a transposed W_down) fails at least
+one of them:
+
+* closed forms at points where tanh and sigmoid are rational (tests/golden/closed_forms.txt);
+* limits and symmetries of the definition;
+* the SwiGLU limit (beta, lbeta -> infinity), a textbook special case;
+* central finite differences of  Λ(x, p) = Σ_r p_r Σ_j g_rj a_rj(x)  for every dx and dp;
+* a brute-force tiny expert  y = Σ_e p_e W_e a_e(x_e)  for the router-gradient rewrite;
+* the definition run under PyTorch autograd in float64 (an independent derivative).
+
+Definition: "Frontier-scale RL with Kimi K3", section "Streaming activations".
+Router rewrite: "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出".
+"""
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _eval(expr: str) -> float:
+    return float(eval(expr, {"__builtins__": {}}, {"log": math.log}))
+
+
+def closed_form_rows():
+    rows = []
+    with open(os.path.join(GOLDEN, "closed_forms.txt")) as f:
+        for line in f:
+            line = line.strip()
+            if not line or line.startswith("#"):
+                continue
+            name, qty, u, v, beta, lbeta, expect = [t.strip() for t in line.split("|")]
+            rows.append((name, qty, _eval(u), _eval(v), float(beta), float(lbeta), _eval(expect)))
+    return rows
+
+
+def pin_closed_forms(o):
+    for row in closed_form_rows():
+        _pin_closed_form_row(o, row)
+
+
+def _pin_closed_form_row(o, row):
+    name, qty, u, v, beta, lbeta, expect = row
+    G, L, Gp, Lp = o.point(u, v, beta, lbeta)
+    got = {"G": G, "L": L, "Gp": Gp, "Lp": Lp}[qty]
+    assert abs(got - expect) <= 1e-13 * max(1.0, abs(expect)), (name, got, expect)
+
+
+def pin_bf16_bits_exact(o):
+    assert o.bf16_to_double(0x3F80) == 1.0
+    assert o.bf16_to_double(0xC000) == -2.0
+    assert o.bf16_to_double(0x3E80) == 0.25
+    z = o.bf16_to_double(0x8000)
+    assert z == 0.0 and math.copysign(1.0, z) == -1.0
+    assert o.bf16_to_double(0x7F7F) == float.fromhex("0x1.fep127")  # bf16 max
+    assert o.bf16_to_double(0x0001) == 2.0 ** -133                   # smallest subnormal
+    assert math.isinf(o.bf16_to_double(0x7F80))
+
+
+def pin_zero_rows(o):
+    # a = G·L vanishes when either half is zero (±0 compare equal; the pages fix no signed-zero rule)
+    # rows are [gate (3) | linear (3)]
+    x = np.array([[0.0, 1.5, -0.0, 3.0, 0.0, 0.0], [2.0, -7.0, 0.5, 0.0, -0.0, 1.0]])
+    out = o.fwd_f64(x)
+    assert out[0, 0] == 0.0 and out[0, 1] == 0.0 and out[0, 2] == 0.0
+    assert out[1, 0] == 0.0 and out[1, 1] == 0.0
+    assert out[1, 2] > 0.0
+
+
+def pin_saturation_limits(o):
+    # G -> beta as u -> +inf (tanh -> 1, sigmoid -> 1); G -> 0- as u -> -inf (≈ -beta·e^u)
+    G, L, Gp, Lp = o.point(80.0, 1000.0)
+    assert G == 4.0 and L == 25.0 and Gp == 0.0 and Lp == 0.0
+    G, L, Gp, Lp = o.point(-80.0, -1000.0)
+    assert G < 0 and abs(G - (-4.0 * math.exp(-80.0))) <= 1e-12 * 4.0 * math.exp(-80.0)
+    assert L == -25.0 and Lp == 0.0
+    assert Gp < 0 and abs(Gp) < 1e-33
+    big = float.fromhex("0x1.fep127")  # largest finite bf16, ~3.39e38
+    for u in (big, -big):
+        for v in (big, -big):
+            G, L, Gp, Lp = o.point(u, v)
+            assert all(math.isfinite(t) for t in (G, L, Gp, Lp))
+            assert G == (4.0 if u > 0 else 0.0)
+            assert L == math.copysign(25.0, v)
+            assert Gp == 0.0 and Lp == 0.0
+    # other beta / lbeta saturate at beta / lbeta
+    G, L, _, _ = o.point(1e4, 1e4, 2.5, 7.0)
+    assert G == 2.5 and L == 7.0
+
+
+def pin_small_argument_expansion(o):
+    # 4 tanh(u/4) = u - u^3/48 + ..., sigmoid(u) = 1/2 + u/4 - u^3/48 + ...
+    # so G(u) = u/2 + u^2/4 - u^3/96 + O(u^4) and G'(u) = 1/2 + u/2 + O(u^2);
+    # L(v) = v + O(v^3), L'(v) = 1 - (v/25)^2 + O(v^4)
+    for u in (1e-4, -1e-4, 3e-6):
+        G, _, Gp, _ = o.point(u, 0.0)
+        assert abs(G - (u / 2 + u * u / 4 - u ** 3 / 96)) <= abs(u) ** 4 + 4e-16 * abs(G)
+        assert abs(Gp - (0.5 + u / 2)) <= abs(u) ** 2
+    for v in (1e-3, -2e-3):
+        _, L, _, Lp = o.point(0.0, v)
+        assert abs(L - v) <= abs(v) ** 3
+        assert abs(Lp - (1 - (v / 25) ** 2)) <= 1e-12
+
+
+def pin_symmetries(o):
+    rng = np.random.default_rng(11)
+    for beta, lbeta in ((4.0, 25.0), (1.5, 3.0), (9.0, 60.0)):
+        for t in np.concatenate([rng.normal(0, 3, 50), rng.uniform(-60, 60, 50)]):
+            t = float(t)
+            Gp_, Lp_, Gpp, Lpp = o.point(t, t, beta, lbeta)
+            Gm, Lm, Gpm, Lpm = o.point(-t, -t, beta, lbeta)
+            # L is odd, L' is even
+            assert Lm == -Lp_ and Lpm == Lpp
+            # sigmoid(u) + sigmoid(-u) = 1  =>  G(u) - G(-u) = beta·tanh(u/beta)
+            #                               =>  G'(u) + G'(-u) = 1 - tanh(u/beta)^2
+            th = math.tanh(t / beta)
+            assert abs((Gp_ - Gm) - beta * th) <= 1e-14 * beta
+            assert abs((Gpp + Gpm) - (1 - th * th)) <= 1e-14
+
+
+def pin_swiglu_limit(o):
+    # beta, lbeta -> inf: beta·tanh(u/beta) -> u and lbeta·tanh(v/lbeta) -> v, so SiTU-GLU
+    # becomes SwiGLU  a = silu(u)·v  with  silu'(u) = sigmoid(u)·(1 + u·(1 - sigmoid(u))).
+    rng = np.random.default_rng(5)
+    for u, v in zip(rng.normal(0, 4, 200), rng.normal(0, 4, 200)):
+        u, v = float(u), float(v)
+        G, L, Gp, Lp = o.point(u, v, 1e8, 1e8)
+        s = 1.0 / (1.0 + math.exp(-u))
+        silu = u * s
+        dsilu = s * (1.0 + u * (1.0 - s))
+        assert abs(G - silu) <= 1e-12 * max(1.0, abs(silu))
+        assert abs(L - v) <= 1e-12 * max(1.0, abs(v))
+        assert abs(Gp - dsilu) <= 1e-12
+        assert abs(Lp - 1.0) <= 1e-12
+
+
+def _lam(o, x, g, p, beta, lbeta):
+    """Λ(x, p) = Σ_r p_r Σ_j g_rj·a_rj(x), with a from the oracle's forward."""
+    a = o.fwd_f64(x, beta, lbeta)
+    return float(np.sum(p[:, None] * g * a))
+
+
+def pin_finite_differences(o, beta=4.0, lbeta=25.0):
+    rng = np.random.default_rng(7)
+    R, H = 3, 5
+    x = rng.normal(0, 3, (R, 2 * H))
+    x[0, 0], x[1, H + 1] = 0.0, -0.0          # include the origin
+    x[2, 1], x[2, H + 2] = -9.0, 40.0         # and a saturating pair
+    g = rng.normal(0, 1, (R, H))
+    p = rng.uniform(0.05, 1, R)
+    dx, dp, dpa = o.bwd_router_f64(x, g, p, beta, lbeta)
+    for r in range(R):
+        for j in range(2 * H):
+            h = 1e-6 * max(1.0, abs(x[r, j]))
+            xp, xm = x.copy(), x.copy()
+            xp[r, j] += h
+            xm[r, j] -= h
+            fd = (_lam(o, xp, g, p, beta, lbeta) - _lam(o, xm, g, p, beta, lbeta)) / (2 * h)
+            assert abs(fd - dx[r, j]) <= 1e-7 * max(1.0, abs(dx[r, j])), (r, j, fd, dx[r, j])
+        # Λ is linear in p_r, so the central difference is exact up to rounding
+        hp = 1e-3
+        pp, pm = p.copy(), p.copy()
+        pp[r] += hp
+        pm[r] -= hp
+        fd = (_lam(o, x, g, pp, beta, lbeta) - _lam(o, x, g, pm, beta, lbeta)) / (2 * hp)
+        assert abs(fd - dp[r]) <= 1e-9 * max(1.0, abs(dp[r]))
+        a = o.fwd_f64(x[r:r + 1], beta, lbeta)[0]
+        assert abs(dpa[r] - np.sum(np.abs(g[r] * a))) <= 1e-12 * dpa[r]
+
+
+def pin_tiny_expert_router_rewrite(o):
+    """y = Σ_e p_e W_e a_e(x_e); loss = <c, y>. The naive router gradient <c, o_e> with the
+    stored expert output o_e = W_e a_e must equal the rewritten <W_eᵀ c, a_e>, which is the
+    oracle's dp with g = W_eᵀ c; and dL/dx_e must equal the oracle's dx with the same g and p_e."""
+    rng = np.random.default_rng(3)
+    D, H, E = 8, 6, 3
+    W = rng.normal(0, 0.5, (E, D, H))
+    xs = rng.normal(0, 3, (E, 2 * H))
+    p = rng.dirichlet(np.ones(E))
+    c = rng.normal(0, 1, D)
+
+    def loss(xs_, p_):
+        a = o.fwd_f64(xs_)
+        y = sum(p_[e] * (W[e] @ a[e]) for e in range(E))
+        return float(c @ y)
+
+    a = o.fwd_f64(xs)
+    g = np.stack([W[e].T @ c for e in range(E)])          # g_e = W_eᵀ dL/dy
+    dx, dp, _ = o.bwd_router_f64(xs, g, p)
+    for e in range(E):
+        o_e = W[e] @ a[e]
+        naive = float(c @ o_e)                               # <dL/dy, o_e>
+        rewritten = float(g[e] @ a[e])                       # <W_eᵀ dL/dy, a_e>
+        assert abs(naive - rewritten) <= 1e-12 * max(1.0, abs(naive))
+        assert abs(dp[e] - naive) <= 1e-12 * max(1.0, abs(naive))
+        hp = 1e-4
+        pp, pm = p.copy(), p.copy()
+        pp[e] += hp
+        pm[e] -= hp
+        fd_p = (loss(xs, pp) - loss(xs, pm)) / (2 * hp)
+        assert abs(fd_p - dp[e]) <= 1e-9 * max(1.0, abs(dp[e]))
+        for j in range(2 * H):
+            h = 1e-6 * max(1.0, abs(xs[e, j]))
+            xp, xm = xs.copy(), xs.copy()
+            xp[e, j] += h
+            xm[e, j] -= h
+            fd = (loss(xp, p) - loss(xm, p)) / (2 * h)
+            assert abs(fd - dx[e, j]) <= 1e-7 * max(1.0, abs(dx[e, j])), (e, j)
+
+
+def _definition_torch(x: torch.Tensor, beta: float, lbeta: float) -> torch.Tensor:
+    """The forward definition written as plain PyTorch ops (float64, CPU) so autograd can
+    differentiate it independently of the oracle's hand-derived G' and L'."""
+    H = x.shape[-1] // 2
+    u, v = x[..., :H], x[..., H:]
+    return torch.tanh(u / beta).mul(beta).mul(torch.sigmoid(u)) * torch.tanh(v / lbeta).mul(lbeta)
+
+
+def pin_autograd_of_definition(o, beta=4.0, lbeta=25.0):
+    gen = torch.Generator().manual_seed(17)
+    R, H = 9, 33
+    x = (torch.randn(R, 2 * H, generator=gen, dtype=torch.float64) * 4).requires_grad_(True)
+    g = torch.randn(R, H, generator=gen, dtype=torch.float64)
+    p = torch.rand(R, generator=gen, dtype=torch.float64).requires_grad_(True)
+    a = _definition_torch(x, beta, lbeta)
+    lam = (p[:, None] * g * a).sum()
+    lam.backward()
+    out_o = o.fwd_f64(x.detach().numpy(), beta, lbeta)
+    dx_o, dp_o, _ = o.bwd_router_f64(x.detach().numpy(), g.numpy(), p.detach().numpy(), beta, lbeta)
+    np.testing.assert_allclose(out_o, a.detach().numpy(), rtol=1e-13, atol=1e-14)
+    np.testing.assert_allclose(dx_o, x.grad.numpy(), rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(dp_o, p.grad.numpy(), rtol=1e-12, atol=1e-13)
+
+
+def pin_bf16_entry_matches_f64_entry(o):
+    rng = np.random.default_rng(1)
+    R, H = 5, 24
+    xb = torch.from_numpy(rng.normal(0, 3, (R, 2 * H)).astype(np.float32)).to(torch.bfloat16)
+    gb = torch.from_numpy(rng.normal(0, 1, (R, H)).astype(np.float32)).to(torch.bfloat16)
+    p = rng.uniform(0, 1, R).astype(np.float32)
+    xbits = xb.view(torch.int16).numpy().view(np.uint16)
+    gbits = gb.view(torch.int16).numpy().view(np.uint16)
+    out_b = o.fwd_bf16(xbits)
+    out_d = o.fwd_f64(xb.to(torch.float64).numpy())
+    assert np.array_equal(out_b, out_d)
+    dx_b, dp_b, dpa_b = o.bwd_router_bf16(xbits, gbits, p)
+    dx_d, dp_d, dpa_d = o.bwd_router_f64(xb.to(torch.float64).numpy(), gb.to(torch.float64).numpy(),
+                                              p.astype(np.float64))
+    assert np.array_equal(dx_b, dx_d) and np.array_equal(dp_b, dp_d) and np.array_equal(dpa_b, dpa_d)
+
+
+def pin_thread_count_independent(o):
+    rng = np.random.default_rng(2)
+    R, H = 37, 40
+    x = rng.normal(0, 3, (R, 2 * H))
+    g = rng.normal(0, 1, (R, H))
+    p = rng.uniform(0, 1, R)
+    r1 = o.bwd_router_f64(x, g, p, nthreads=1)
+    r5 = o.bwd_router_f64(x, g, p, nthreads=5)
+    for a, b in zip(r1, r5):
+        assert np.array_equal(a, b)
+    assert np.array_equal(o.fwd_f64(x, nthreads=1), o.fwd_f64(x, nthreads=7))
+
+
+def pin_extreme_finite_inputs(o):
+    big = float.fromhex("0x1.fep127")
+    x = np.array([[big, -big, 0.0, big, -big, 1.0, 3.0, -big]])
+    g = np.array([[1.0, -2.0, 0.5, 3.0]])
+    p = np.array([0.7])
+    dx, dp, dpa = o.bwd_router_f64(x, g, p)
+    assert np.all(np.isfinite(dx)) and np.isfinite(dp).all() and np.isfinite(dpa).all()
+    out = o.fwd_f64(x)
+    assert np.all(np.isfinite(out))
+    # u = +big: G = 4; v = -big: L = -25  ->  a = -100
+    assert out[0, 0] == -100.0
+
+
+def pin_empty_rows(o):
+    out = o.fwd_f64(np.zeros((0, 8)))
+    assert out.shape == (0, 4)
+    dx, dp, dpa = o.bwd_router_f64(np.zeros((0, 8)), np.zeros((0, 4)), np.zeros((0,)))
+    assert dx.shape == (0, 8) and dp.shape == (0,)

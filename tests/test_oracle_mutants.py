@@ -1,0 +1,78 @@
+"""The oracle's pins are sensitive: each plausible mistake, planted in a copy of the oracle
+source and compiled on the CPU, must make at least one pin fail.
+
+Mutations only change arithmetic or in-bounds indexing (no out-of-range access).
+An unmodified copy compiled the same way must pass every pin (control).
+"""
+import numpy as np
+import pytest
+
+import _pins
+import oracle
+
+PINS = [
+    ("closed_forms", _pins.pin_closed_forms),
+    ("bf16_bits", _pins.pin_bf16_bits_exact),
+    ("zero_rows", _pins.pin_zero_rows),
+    ("saturation", _pins.pin_saturation_limits),
+    ("small_argument", _pins.pin_small_argument_expansion),
+    ("symmetries", _pins.pin_symmetries),
+    ("swiglu_limit", _pins.pin_swiglu_limit),
+    ("fd_4_25", lambda o: _pins.pin_finite_differences(o, 4.0, 25.0)),
+    ("fd_2_5", lambda o: _pins.pin_finite_differences(o, 2.0, 5.0)),
+    ("tiny_expert", _pins.pin_tiny_expert_router_rewrite),
+    ("autograd", lambda o: _pins.pin_autograd_of_definition(o, 4.0, 25.0)),
+    ("bf16_vs_f64", _pins.pin_bf16_entry_matches_f64_entry),
+    ("extreme", _pins.pin_extreme_finite_inputs),
+]
+
+MUTANTS = {
+    "drop_second_term_of_Gprime": ("double Gp = (1.0 - T * T) * S + beta * T * S * (1.0 - S);",
+                                   "double Gp = (1.0 - T * T) * S;"),
+    "wrong_sign_in_Gprime": ("(1.0 - T * T) * S + beta * T * S * (1.0 - S)",
+                             "(1.0 - T * T) * S - beta * T * S * (1.0 - S)"),
+    "sigmoid_negative_branch": ("return e / (1.0 + e);", "return 1.0 / (1.0 + e);"),
+    "sigmoid_positive_sign": ("return 1.0 / (1.0 + exp(-u));", "return 1.0 / (1.0 + exp(u));"),
+    "gate_linear_swapped": ("oracle_situ_point(xr[j], xr[H + j],", "oracle_situ_point(xr[H + j], xr[j],"),
+    "p_folded_into_dp": ("acc += gr[j] * a;", "acc += p * gr[j] * a;"),
+    "dx_without_p": ("dxr[j] = p * gr[j] * L * Gp;", "dxr[j] = gr[j] * L * Gp;"),
+    "dgate_dlinear_swapped": ("dxr[j] = p * gr[j] * L * Gp;\n        dxr[H + j] = p * gr[j] * G * Lp;",
+                              "dxr[j] = p * gr[j] * G * Lp;\n        dxr[H + j] = p * gr[j] * L * Gp;"),
+    "Lprime_not_squared": ("double Lp = 1.0 - W * W;", "double Lp = 1.0 - W;"),
+    "gate_missing_beta": ("double G = beta * T * S;", "double G = T * S;"),
+    "tanh_argument_inverted": ("double T = tanh(u / beta);", "double T = tanh(u * beta);"),
+    "linear_missing_lbeta": ("double L = lbeta * W;", "double L = W;"),
+    "linear_uses_beta": ("double W = tanh(v / lbeta);", "double W = tanh(v / beta);"),
+    "dp_abs_not_absolute": ("acc_abs += fabs(gr[j] * a);", "acc_abs += gr[j] * a;"),
+    "bf16_shift_wrong": ("((uint32_t)bits) << 16;", "((uint32_t)bits) << 15;"),
+    "bf16_row_stride_wrong": ("(const uint16_t*)jb->x + r * 2 * H;", "(const uint16_t*)jb->x + r * H;"),
+    "bf16_p_index_wrong": ("p = (double)((const float*)jb->p)[r];", "p = (double)((const float*)jb->p)[0];"),
+    "g_row_off_by_one": ("gr = (const double*)jb->g + r * H;",
+                         "gr = (const double*)jb->g + (r > 0 ? r - 1 : 0) * H;"),
+}
+
+
+def failing_pins(o):
+    failed = []
+    with np.errstate(all="ignore"):
+        for name, pin in PINS:
+            try:
+                pin(o)
+            except AssertionError:
+                failed.append(name)
+    return failed
+
+
+def test_unmodified_copy_passes_every_pin(tmp_path):
+    o = oracle.compile_variant(oracle.source_text(), str(tmp_path / "control.so"))
+    assert failing_pins(o) == []
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_planted_mistake_is_caught(tmp_path, name):
+    find, repl = MUTANTS[name]
+    text = oracle.source_text()
+    assert find in text, f"mutation anchor not found: {name}"
+    o = oracle.compile_variant(text.replace(find, repl), str(tmp_path / f"{name}.so"))
+    failed = failing_pins(o)
+    assert failed, f"no pin catches the planted mistake {name}"
