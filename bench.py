@@ -38,10 +38,10 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum), per row, and the hash of the kernel source it was taken on.
 # Reported only while the source is unchanged; otherwise null.
 NCU_TRAFFIC = {
-    "source_sha256": None,
-    "bwd_bytes_per_row": None,
-    "fwd_bytes_per_row": None,
-    "capture": None,
+    "source_sha256": "9f7c664e56b8cbb9fe2c8fd53fdf809a8de15e2f365bf7b3ddd9b290ef62cdca",
+    "bwd_bytes_per_row": (1.208400e9 + 0.7679488e9) / 65536,
+    "fwd_bytes_per_row": (0.805347e9 + 0.365363712e9) / 65536,
+    "capture": "ncu --set full, R=65536 H=3072, scaled by rows (profiles/situ_glu_fwd_bwd_ncu_full_r65536_h3072.md)",
 }
 
 
@@ -311,6 +311,7 @@ def run_native(args):
     barrier(world)
     torch.cuda.synchronize(dev)
     sampler.start()
+    torch.cuda.nvtx.range_push("timed")
     start.record(stream)
     for i in range(K):
         ev[i][0].record(stream)
@@ -320,6 +321,7 @@ def run_native(args):
                                    R, H, 4.0, 25.0, sh)
         ev[i][2].record(stream)
     end.record(stream)
+    torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize(dev)
     clocks = sampler.stop()
     barrier(world)
@@ -381,7 +383,8 @@ def run_native(args):
                      "achieved": bwd_gbs, "peak": peak, "unit": "GB/s", "frac": bwd_gbs / peak,
                      "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
-                     "algorithmic_bytes_per_launch": bwd_bytes, "traffic": traffic},
+                     "algorithmic_bytes_per_launch": bwd_bytes, "traffic": traffic,
+                     "traffic_source": NCU_TRAFFIC["capture"] if traffic is not None else None},
         "clocks": clocks,
         "gpu_launches": 2 * K,
         "e2e": e2e,
@@ -395,10 +398,15 @@ def run_native(args):
 
 
 def pinned_like(t):
-    """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size)."""
+    """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size, touched).
+
+    Registered portable | mapped (flags 3): on this platform device->host copies into memory
+    registered with flags 0 ran at ~31 GB/s against ~190 GB/s with these flags."""
     import torch
     h = torch.empty(t.shape, dtype=t.dtype)
-    rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 0)
+    if h.numel():
+        h.view(-1).view(torch.uint8).zero_()
+    rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 3)
     if int(rc) != 0:
         raise RuntimeError(f"cudaHostRegister failed: {rc}")
     return h
@@ -409,9 +417,13 @@ def unpin(h):
     torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
 
 
-def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world):
-    """Same step through the public binding with inputs copied in from pinned host memory and
-    every result copied back, inside the timed region."""
+def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_rows=65536):
+    """The step through the public binding with every input copied in from page-locked host
+    memory and every result copied back, inside the timed region.
+
+    Rows are independent, so the step streams over row chunks on three CUDA streams:
+    host->device copies of chunk i+1 and device->host copies of chunk i-1 overlap the kernels
+    of chunk i. Events order the reuse of each chunk's device rows across steps."""
     import torch
     steps = max(1, steps)
     xh, gh, ph, oh, dxh, dph = (pinned_like(t) for t in (x, g, p, out, dx, dp))
@@ -420,28 +432,56 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world):
     ph.copy_(p)
     h2d = xh.numel() * 2 + gh.numel() * 2 + ph.numel() * 4
     d2h = oh.numel() * 2 + dxh.numel() * 2 + dph.numel() * 4
+    s_in, s_cmp, s_out = torch.cuda.Stream(dev), stream, torch.cuda.Stream(dev)
+    bounds = [(r0, min(R, r0 + chunk_rows)) for r0 in range(0, R, chunk_rows)]
+    n = len(bounds)
+    computed = [None] * n   # event: kernels of chunk i done (its x/g/p may be overwritten)
+    drained = [None] * n    # event: results of chunk i copied out (its out/dx/dp may be overwritten)
+    launches = [0]
 
-    def one():
-        with torch.cuda.stream(stream):
-            x.copy_(xh, non_blocking=True)
-            g.copy_(gh, non_blocking=True)
-            p.copy_(ph, non_blocking=True)
-            sg.situ_glu_fwd(x, out, stream=stream)
-            sg.situ_glu_bwd_router(x, g, p, dx, dp, stream=stream)
-            oh.copy_(out, non_blocking=True)
-            dxh.copy_(dx, non_blocking=True)
-            dph.copy_(dp, non_blocking=True)
+    def one_step():
+        for i, (a, b) in enumerate(bounds):
+            with torch.cuda.stream(s_in):
+                if computed[i] is not None:
+                    s_in.wait_event(computed[i])
+                x[a:b].copy_(xh[a:b], non_blocking=True)
+                g[a:b].copy_(gh[a:b], non_blocking=True)
+                p[a:b].copy_(ph[a:b], non_blocking=True)
+                loaded = torch.cuda.Event()
+                loaded.record(s_in)
+            s_cmp.wait_event(loaded)
+            if drained[i] is not None:
+                s_cmp.wait_event(drained[i])
+            sg.situ_glu_fwd(x[a:b], out[a:b], stream=s_cmp)
+            sg.situ_glu_bwd_router(x[a:b], g[a:b], p[a:b], dx[a:b], dp[a:b], stream=s_cmp)
+            launches[0] += 2
+            done = torch.cuda.Event()
+            done.record(s_cmp)
+            computed[i] = done
+            s_out.wait_event(done)
+            with torch.cuda.stream(s_out):
+                oh[a:b].copy_(out[a:b], non_blocking=True)
+                dxh[a:b].copy_(dx[a:b], non_blocking=True)
+                dph[a:b].copy_(dp[a:b], non_blocking=True)
+                ev = torch.cuda.Event()
+                ev.record(s_out)
+            drained[i] = ev
 
-    one()
+    one_step()
     torch.cuda.synchronize(dev)
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
     barrier(world)
     torch.cuda.synchronize(dev)
-    start.record(stream)
+    launches[0] = 0
+    start.record(s_in)
+    s_cmp.wait_event(start)
+    s_out.wait_event(start)
     for _ in range(steps):
-        one()
-    end.record(stream)
+        one_step()
+    s_out.wait_stream(s_in)
+    s_out.wait_stream(s_cmp)
+    end.record(s_out)
     torch.cuda.synchronize(dev)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world, dev)
@@ -449,7 +489,9 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world):
         unpin(t)
     return {"value": whole_job_rate(R, world, steps, ms * 1e-3), "unit": "rows/s", "steps": steps,
             "ms_per_step": ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-            "how": "pinned host x,g,p -> device, fwd + bwd via the binding, out,dx,dp -> pinned host; one stream"}
+            "gpu_launches": launches[0],
+            "how": f"page-locked host x,g,p -> device -> fwd + bwd via the binding -> out,dx,dp -> host, "
+                   f"streamed over {n} row chunks of {chunk_rows} on 3 CUDA streams"}
 
 
 def main(argv=None):

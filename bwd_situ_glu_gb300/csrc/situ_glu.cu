@@ -7,13 +7,16 @@
 // There is no contraction, so no tensor cores. Design:
 //   * one warp per row, rows distributed grid-stride over a persistent grid sized
 //     from the SM count and the kernel's occupancy;
-//   * each lane moves 16-byte vectors (8 bf16); a warp instruction covers 512
-//     contiguous bytes; UNROLL chunks per lane are loaded before any math so
-//     every warp has several KB in flight;
-//   * all intermediates (the "constant fp32 workspace" of the pages' custom
-//     operator) live in registers: nothing but x, g, p, out, dx, dp touches memory;
-//   * dp is a fixed-order per-lane fp32 sum followed by a butterfly shuffle, so
-//     results are bit-reproducible.
+//   * each lane moves 16-byte vectors (8 bf16), or 32-byte vectors (one ld/st.global.v8) in the
+//     backward when H % 16 == 0 and the bases are 32-byte aligned; a warp instruction covers
+//     512 B or 1 KB of contiguous memory, and U chunks per lane are loaded before any math;
+//   * the launch shapes were chosen by measurement on GB300 with HBM-resident inputs: both
+//     directions run one 1024-thread CTA per SM (32 warps on 32 consecutive rows), except the
+//     forward for H not a multiple of 512, which runs six 128-thread CTAs per SM;
+//   * all intermediates (the "constant fp32 workspace" of the pages' custom operator) live
+//     in registers: nothing but x, g, p, out, dx, dp touches memory;
+//   * dp is a fixed-order per-lane fp32 sum followed by a butterfly shuffle, so results are
+//     bit-reproducible.
 // Sources: "Frontier-scale RL with Kimi K3", section "Streaming activations";
 // "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出".
 #include <cuda_runtime.h>
@@ -33,28 +36,64 @@ using situ::Coef;
 // memory helpers (inline PTX)
 // ---------------------------------------------------------------------------
 
-// Streaming 16-byte load through the non-coherent path (inputs that no thread writes).
-__device__ __forceinline__ uint4 ld_nc(const uint4* p) {
-    uint4 v;
-    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
+// NW consecutive 32-bit words (2·NW bf16): NW = 4 is a 16-byte chunk, NW = 8 a 32-byte chunk.
+template <int NW>
+struct Vec {
+    uint32_t w[NW];
+};
+
+// Streaming load. NC = true reads through the non-coherent path (inputs no thread writes);
+// NC = false through the coherent path (x, which dx may alias in place). NOALLOC adds the
+// L1::no_allocate hint (measured faster for the 32-byte backward, slower for the 16-byte one).
+template <int NW, bool NC, bool NOALLOC = true>
+__device__ __forceinline__ Vec<NW> ld_stream(const Vec<NW>* p) {
+    Vec<NW> v;
+    if constexpr (NW == 4) {
+        if constexpr (NC && NOALLOC)
+            asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                : "l"(p));
+        else if constexpr (NC)
+            asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                : "l"(p));
+        else if constexpr (NOALLOC)
+            asm("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                : "l"(p));
+        else
+            asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+                : "l"(p));
+    } else {
+        static_assert(NW == 8, "16- or 32-byte vectors");
+        static_assert(NOALLOC, "the 32-byte path always uses L1::no_allocate");
+        if constexpr (NC)
+            asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                  "=r"(v.w[6]), "=r"(v.w[7])
+                : "l"(p));
+        else
+            asm("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
+                  "=r"(v.w[6]), "=r"(v.w[7])
+                : "l"(p));
+    }
     return v;
 }
 
-// Streaming 16-byte load through the coherent path (x may alias dx in the backward).
-__device__ __forceinline__ uint4 ld_co(const uint4* p) {
-    uint4 v;
-    asm("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-        : "l"(p));
-    return v;
-}
-
-// Streaming (evict-first) 16-byte store.
-__device__ __forceinline__ void st_cs(uint4* p, uint4 v) {
-    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
+// Streaming (evict-first) store.
+template <int NW>
+__device__ __forceinline__ void st_stream(Vec<NW>* p, const Vec<NW>& v) {
+    if constexpr (NW == 4) {
+        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
+                     "r"(v.w[3])
+                     : "memory");
+    } else {
+        asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
+                     "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
+                     : "memory");
+    }
 }
 
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -80,57 +119,57 @@ __device__ __forceinline__ float warp_sum(float v) {
 // forward kernels
 // ---------------------------------------------------------------------------
 
-constexpr int kThreads = 256;           // 8 warps per CTA
-constexpr int kWarps = kThreads / 32;
-
-// Vector path: H % 8 == 0, x and out 16-byte aligned. cpr = H / 8 chunks per half-row.
-template <bool BETA4, int UNROLL>
-__global__ void __launch_bounds__(kThreads) fwd_vec_kernel(const uint4* __restrict__ x, uint4* __restrict__ out,
-                                                           int64_t R, int cpr, Coef c) {
+// Vector path. cpr = chunks of NW words per half-row (H = 2·NW·cpr); the launch shape S gives
+// NW, U (chunks per lane loaded before the math), TPB (threads per CTA) and MINB (resident
+// CTAs per SM requested from the register allocator).
+template <bool BETA4, class S, int NW = S::NW, int U = S::U, int TPB = S::TPB>
+__global__ void __launch_bounds__(S::TPB, S::MINB) fwd_vec_kernel(const Vec<NW>* __restrict__ x, Vec<NW>* __restrict__ out,
+                                                            int64_t R, int cpr, Coef c) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t warp0 = ((int64_t)blockIdx.x * TPB + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * TPB) >> 5;
     for (int64_t r = warp0; r < R; r += nwarps) {
-        const uint4* xg = x + r * (2 * (int64_t)cpr);
-        const uint4* xl = xg + cpr;
-        uint4* o = out + r * (int64_t)cpr;
-        for (int c0 = 0; c0 < cpr; c0 += 32 * UNROLL) {
-            uint4 gv[UNROLL], lv[UNROLL];
+        const Vec<NW>* xg = x + r * (2 * (int64_t)cpr);
+        const Vec<NW>* xl = xg + cpr;
+        Vec<NW>* o = out + r * (int64_t)cpr;
+        for (int c0 = 0; c0 < cpr; c0 += 32 * U) {
+            Vec<NW> gv[U], lv[U];
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ci = c0 + k * 32 + lane;
                 if (ci < cpr) {
-                    gv[k] = ld_nc(xg + ci);
-                    lv[k] = ld_nc(xl + ci);
+                    gv[k] = ld_stream<NW, true, S::NOALLOC>(xg + ci);
+                    lv[k] = ld_stream<NW, true, S::NOALLOC>(xl + ci);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ci = c0 + k * 32 + lane;
                 if (ci < cpr) {
-                    const uint32_t gw[4] = {gv[k].x, gv[k].y, gv[k].z, gv[k].w};
-                    const uint32_t lw[4] = {lv[k].x, lv[k].y, lv[k].z, lv[k].w};
-                    uint32_t ow[4];
+                    Vec<NW> ov;
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float a0 = situ::fwd<BETA4>(bf16_lo(gw[i]), bf16_lo(lw[i]), c);
-                        float a1 = situ::fwd<BETA4>(bf16_hi(gw[i]), bf16_hi(lw[i]), c);
-                        ow[i] = pack_bf16x2(a0, a1);
+                    for (int i = 0; i < NW; ++i) {
+                        float a0 = situ::fwd<BETA4>(bf16_lo(gv[k].w[i]), bf16_lo(lv[k].w[i]), c);
+                        float a1 = situ::fwd<BETA4>(bf16_hi(gv[k].w[i]), bf16_hi(lv[k].w[i]), c);
+                        ov.w[i] = pack_bf16x2(a0, a1);
                     }
-                    st_cs(o + ci, make_uint4(ow[0], ow[1], ow[2], ow[3]));
+                    st_stream<NW>(o + ci, ov);
                 }
             }
         }
     }
 }
 
+constexpr int kElemThreads = 256;
+
 // Element path: any H, any 2-byte-aligned pointers.
 template <bool BETA4>
-__global__ void __launch_bounds__(kThreads) fwd_elem_kernel(const uint16_t* __restrict__ x, uint16_t* __restrict__ out,
-                                                            int64_t R, int64_t H, Coef c) {
+__global__ void __launch_bounds__(kElemThreads) fwd_elem_kernel(const uint16_t* __restrict__ x,
+                                                                uint16_t* __restrict__ out, int64_t R, int64_t H,
+                                                                Coef c) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t warp0 = ((int64_t)blockIdx.x * kElemThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kElemThreads) >> 5;
     for (int64_t r = warp0; r < R; r += nwarps) {
         const uint16_t* xr = x + r * 2 * H;
         uint16_t* orow = out + r * H;
@@ -145,64 +184,59 @@ __global__ void __launch_bounds__(kThreads) fwd_elem_kernel(const uint16_t* __re
 // backward + router-gradient kernels
 // ---------------------------------------------------------------------------
 
-template <bool BETA4>
-__device__ __forceinline__ void bwd_chunk(const uint4& gv, const uint4& lv, const uint4& dv, float p, const Coef& c,
-                                          float& acc, uint4& dgo, uint4& dlo) {
-    const uint32_t gw[4] = {gv.x, gv.y, gv.z, gv.w};
-    const uint32_t lw[4] = {lv.x, lv.y, lv.z, lv.w};
-    const uint32_t yw[4] = {dv.x, dv.y, dv.z, dv.w};
-    uint32_t dg[4], dl[4];
+// One chunk: NW words of gate, linear and g -> dgate, dlinear; accumulates g·a into acc.
+template <bool BETA4, int NW>
+__device__ __forceinline__ void bwd_chunk(const Vec<NW>& gv, const Vec<NW>& lv, const Vec<NW>& yv, float p,
+                                          const Coef& c, float& acc, Vec<NW>& dgo, Vec<NW>& dlo) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        float g0 = bf16_lo(yw[i]), g1 = bf16_hi(yw[i]);
-        situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gw[i]), bf16_lo(lw[i]), p * g0, c);
-        situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gw[i]), bf16_hi(lw[i]), p * g1, c);
+    for (int i = 0; i < NW; ++i) {
+        float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
+        situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gv.w[i]), bf16_lo(lv.w[i]), p * g0, c);
+        situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gv.w[i]), bf16_hi(lv.w[i]), p * g1, c);
         acc = fmaf(g0, b0.a, acc);
         acc = fmaf(g1, b1.a, acc);
-        dg[i] = pack_bf16x2(b0.dgate, b1.dgate);
-        dl[i] = pack_bf16x2(b0.dlin, b1.dlin);
+        dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
+        dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
     }
-    dgo = make_uint4(dg[0], dg[1], dg[2], dg[3]);
-    dlo = make_uint4(dl[0], dl[1], dl[2], dl[3]);
 }
 
-// Vector path: H % 8 == 0; x, g, dx 16-byte aligned. dx may equal x (in place): every
-// 16-byte chunk of x is loaded by the lane that later stores the same chunk of dx, and
-// no thread reads a chunk after it was written, so x is read through the coherent path.
-template <bool BETA4, int UNROLL>
-__global__ void __launch_bounds__(kThreads) bwd_vec_kernel(const uint4* x, const uint4* __restrict__ g,
-                                                           const float* __restrict__ p, uint4* dx,
-                                                           float* __restrict__ dp, int64_t R, int cpr, Coef c) {
+// Vector path. dx may equal x (in place): every chunk of x is loaded by the lane that later
+// stores the same chunk of dx, and no thread reads a chunk after it was written, so x is
+// read through the coherent path.
+template <bool BETA4, class S, int NW = S::NW, int U = S::U, int TPB = S::TPB>
+__global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<NW>* x, const Vec<NW>* __restrict__ g,
+                                                            const float* __restrict__ p, Vec<NW>* dx,
+                                                            float* __restrict__ dp, int64_t R, int cpr, Coef c) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t warp0 = ((int64_t)blockIdx.x * TPB + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * TPB) >> 5;
     for (int64_t r = warp0; r < R; r += nwarps) {
-        const uint4* xg = x + r * (2 * (int64_t)cpr);
-        const uint4* xl = xg + cpr;
-        const uint4* gr = g + r * (int64_t)cpr;
-        uint4* dgr = dx + r * (2 * (int64_t)cpr);
-        uint4* dlr = dgr + cpr;
+        const Vec<NW>* xg = x + r * (2 * (int64_t)cpr);
+        const Vec<NW>* xl = xg + cpr;
+        const Vec<NW>* gr = g + r * (int64_t)cpr;
+        Vec<NW>* dgr = dx + r * (2 * (int64_t)cpr);
+        Vec<NW>* dlr = dgr + cpr;
         const float pr = p[r];
         float acc = 0.0f;
-        for (int c0 = 0; c0 < cpr; c0 += 32 * UNROLL) {
-            uint4 gv[UNROLL], lv[UNROLL], yv[UNROLL];
+        for (int c0 = 0; c0 < cpr; c0 += 32 * U) {
+            Vec<NW> gv[U], lv[U], yv[U];
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ci = c0 + k * 32 + lane;
                 if (ci < cpr) {
-                    gv[k] = ld_co(xg + ci);
-                    lv[k] = ld_co(xl + ci);
-                    yv[k] = ld_nc(gr + ci);
+                    gv[k] = ld_stream<NW, false, S::NOALLOC>(xg + ci);
+                    lv[k] = ld_stream<NW, false, S::NOALLOC>(xl + ci);
+                    yv[k] = ld_stream<NW, true, S::NOALLOC>(gr + ci);
                 }
             }
 #pragma unroll
-            for (int k = 0; k < UNROLL; ++k) {
+            for (int k = 0; k < U; ++k) {
                 const int ci = c0 + k * 32 + lane;
                 if (ci < cpr) {
-                    uint4 dgo, dlo;
-                    bwd_chunk<BETA4>(gv[k], lv[k], yv[k], pr, c, acc, dgo, dlo);
-                    st_cs(dgr + ci, dgo);
-                    st_cs(dlr + ci, dlo);
+                    Vec<NW> dgo, dlo;
+                    bwd_chunk<BETA4, NW>(gv[k], lv[k], yv[k], pr, c, acc, dgo, dlo);
+                    st_stream<NW>(dgr + ci, dgo);
+                    st_stream<NW>(dlr + ci, dlo);
                 }
             }
         }
@@ -214,12 +248,13 @@ __global__ void __launch_bounds__(kThreads) bwd_vec_kernel(const uint4* x, const
 // Element path: any H, any 2-byte-aligned bf16 pointers. dx may equal x (each element is
 // read and then written by the same lane).
 template <bool BETA4>
-__global__ void __launch_bounds__(kThreads) bwd_elem_kernel(const uint16_t* x, const uint16_t* __restrict__ g,
-                                                            const float* __restrict__ p, uint16_t* dx,
-                                                            float* __restrict__ dp, int64_t R, int64_t H, Coef c) {
+__global__ void __launch_bounds__(kElemThreads) bwd_elem_kernel(const uint16_t* x, const uint16_t* __restrict__ g,
+                                                                const float* __restrict__ p, uint16_t* dx,
+                                                                float* __restrict__ dp, int64_t R, int64_t H,
+                                                                Coef c) {
     const int lane = threadIdx.x & 31;
-    const int64_t warp0 = ((int64_t)blockIdx.x * kThreads + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * kThreads) >> 5;
+    const int64_t warp0 = ((int64_t)blockIdx.x * kElemThreads + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * kElemThreads) >> 5;
     for (int64_t r = warp0; r < R; r += nwarps) {
         const uint16_t* xr = x + r * 2 * H;
         const uint16_t* gr = g + r * H;
@@ -244,8 +279,32 @@ __global__ void __launch_bounds__(kThreads) bwd_elem_kernel(const uint16_t* x, c
 // host side: validation, launch configuration, errors
 // ---------------------------------------------------------------------------
 
-constexpr int kFwdUnroll = 4;
-constexpr int kBwdUnroll = 4;
+// Launch shapes: vector width in 32-bit words (4 = 16 B, 8 = 32 B), chunks per lane, threads
+// per CTA, min CTAs per SM, L1::no_allocate on loads. Chosen by measurement on GB300 with
+// HBM-resident inputs (R = 1.6M x H = 3072, R = 524288 x H in {3584, 1000}): warps of one
+// 1024-thread CTA per SM work on 32 consecutive rows, which the memory system served best.
+struct Fwd16Big {    // H % 512 == 0: two 16-byte chunks per lane tile the row exactly
+    static constexpr int NW = 4, U = 2, TPB = 1024, MINB = 1;
+    static constexpr bool NOALLOC = true;
+};
+struct Fwd16 {       // other H % 8 == 0
+    static constexpr int NW = 4, U = 4, TPB = 128, MINB = 6;
+    static constexpr bool NOALLOC = true;
+};
+struct Bwd32 {       // H % 16 == 0, 32-byte aligned bases
+    static constexpr int NW = 8, U = 1, TPB = 1024, MINB = 1;
+    static constexpr bool NOALLOC = true;
+};
+struct Bwd16 {       // other H % 8 == 0
+    static constexpr int NW = 4, U = 2, TPB = 1024, MINB = 1;
+    static constexpr bool NOALLOC = false;
+};
+
+enum KernelId {
+    K_FWD16BIG_B4, K_FWD16BIG_GEN, K_FWD16_B4, K_FWD16_GEN, K_FWDE_B4, K_FWDE_GEN,
+    K_BWD32_B4, K_BWD32_GEN, K_BWD16_B4, K_BWD16_GEN, K_BWDE_B4, K_BWDE_GEN,
+    K_COUNT
+};
 
 thread_local int t_last_cuda_error = 0;
 
@@ -289,7 +348,7 @@ Range range_of(const void* p, int64_t bytes) {
 
 bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
 
-// Shared checks of R, H, beta, lbeta; sets *elems2 = R*2H when valid.
+// Shared checks of R, H, beta, lbeta.
 int check_shape(int64_t R, int64_t H, float beta, float lbeta) {
     if (R < 0 || H <= 0 || H > SITU_GLU_MAX_H) return SITU_GLU_INVALID_ARG;
     if (!finite_positive(beta) || !finite_positive(lbeta)) return SITU_GLU_INVALID_ARG;
@@ -300,12 +359,11 @@ int check_shape(int64_t R, int64_t H, float beta, float lbeta) {
 
 // Per-device launch configuration cache: SM count and resident CTAs per SM for each kernel.
 constexpr int kMaxDevices = 64;
-constexpr int kNumKernels = 8;
 std::mutex g_cfg_mutex;
 int g_sm_count[kMaxDevices];
-int g_blocks_per_sm[kMaxDevices][kNumKernels];
+int g_blocks_per_sm[kMaxDevices][K_COUNT];
 
-int grid_for(int kernel_id, const void* fn, int64_t R, int* grid) {
+int grid_for(int kernel_id, const void* fn, int tpb, int64_t R, int* grid) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e);
@@ -321,7 +379,7 @@ int grid_for(int kernel_id, const void* fn, int64_t R, int* grid) {
         }
         if (g_blocks_per_sm[dev][kernel_id] == 0) {
             int b = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, kThreads, 0);
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, tpb, 0);
             if (e != cudaSuccess) return cuda_fail(e);
             g_blocks_per_sm[dev][kernel_id] = b > 0 ? b : 1;
         }
@@ -329,20 +387,35 @@ int grid_for(int kernel_id, const void* fn, int64_t R, int* grid) {
         per_sm = g_blocks_per_sm[dev][kernel_id];
     }
     const int64_t persistent = (int64_t)sms * per_sm;
-    const int64_t needed = (R + kWarps - 1) / kWarps;  // one warp per row
+    const int64_t warps_per_cta = tpb / 32;
+    const int64_t needed = (R + warps_per_cta - 1) / warps_per_cta;  // one warp per row
     *grid = (int)(needed < persistent ? needed : persistent);
     return SITU_GLU_OK;
 }
 
 template <typename Kernel, typename... Args>
-int launch(int kernel_id, Kernel kernel, int64_t R, cudaStream_t stream, Args... args) {
+int launch(int kernel_id, Kernel kernel, int tpb, int64_t R, cudaStream_t stream, Args... args) {
     int grid = 0;
-    int st = grid_for(kernel_id, (const void*)kernel, R, &grid);
+    int st = grid_for(kernel_id, (const void*)kernel, tpb, R, &grid);
     if (st != SITU_GLU_OK) return st;
-    kernel<<<grid, kThreads, 0, stream>>>(args...);
+    kernel<<<grid, tpb, 0, stream>>>(args...);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return SITU_GLU_OK;
+}
+
+template <bool B4, class S>
+int launch_fwd(int id, const void* x, void* out, int64_t R, int64_t H, const Coef& c, cudaStream_t stream) {
+    const int cpr = (int)(H / (2 * S::NW));
+    return launch(id, fwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (Vec<S::NW>*)out, R, cpr, c);
+}
+
+template <bool B4, class S>
+int launch_bwd(int id, const void* x, const void* g, const float* p, void* dx, float* dp, int64_t R, int64_t H,
+               const Coef& c, cudaStream_t stream) {
+    const int cpr = (int)(H / (2 * S::NW));
+    return launch(id, bwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (const Vec<S::NW>*)g, p,
+                  (Vec<S::NW>*)dx, dp, R, cpr, c);
 }
 
 }  // namespace
@@ -360,18 +433,17 @@ int situ_glu_fwd(const void* x, void* out, int64_t R, int64_t H, float beta, flo
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
-    const bool vec = (H % 8 == 0) && aligned(x, 16) && aligned(out, 16);
-    if (vec) {
-        const int cpr = (int)(H / 8);
-        const uint4* xv = (const uint4*)x;
-        uint4* ov = (uint4*)out;
-        if (b4) return launch(0, fwd_vec_kernel<true, kFwdUnroll>, R, stream, xv, ov, R, cpr, c);
-        return launch(1, fwd_vec_kernel<false, kFwdUnroll>, R, stream, xv, ov, R, cpr, c);
+    if (H % 8 == 0 && aligned(x, 16) && aligned(out, 16)) {
+        if (H % 512 == 0)
+            return b4 ? launch_fwd<true, Fwd16Big>(K_FWD16BIG_B4, x, out, R, H, c, stream)
+                      : launch_fwd<false, Fwd16Big>(K_FWD16BIG_GEN, x, out, R, H, c, stream);
+        return b4 ? launch_fwd<true, Fwd16>(K_FWD16_B4, x, out, R, H, c, stream)
+                  : launch_fwd<false, Fwd16>(K_FWD16_GEN, x, out, R, H, c, stream);
     }
     const uint16_t* xs = (const uint16_t*)x;
     uint16_t* os = (uint16_t*)out;
-    if (b4) return launch(2, fwd_elem_kernel<true>, R, stream, xs, os, R, H, c);
-    return launch(3, fwd_elem_kernel<false>, R, stream, xs, os, R, H, c);
+    if (b4) return launch(K_FWDE_B4, fwd_elem_kernel<true>, kElemThreads, R, stream, xs, os, R, H, c);
+    return launch(K_FWDE_GEN, fwd_elem_kernel<false>, kElemThreads, R, stream, xs, os, R, H, c);
 }
 
 int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, float* dp, int64_t R, int64_t H,
@@ -391,20 +463,19 @@ int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, 
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
-    const bool vec = (H % 8 == 0) && aligned(x, 16) && aligned(g, 16) && aligned(dx, 16);
-    if (vec) {
-        const int cpr = (int)(H / 8);
-        const uint4* xv = (const uint4*)x;
-        const uint4* gv = (const uint4*)g;
-        uint4* dxv = (uint4*)dx;
-        if (b4) return launch(4, bwd_vec_kernel<true, kBwdUnroll>, R, stream, xv, gv, p, dxv, dp, R, cpr, c);
-        return launch(5, bwd_vec_kernel<false, kBwdUnroll>, R, stream, xv, gv, p, dxv, dp, R, cpr, c);
+    if (H % 16 == 0 && aligned(x, 32) && aligned(g, 32) && aligned(dx, 32)) {
+        return b4 ? launch_bwd<true, Bwd32>(K_BWD32_B4, x, g, p, dx, dp, R, H, c, stream)
+                  : launch_bwd<false, Bwd32>(K_BWD32_GEN, x, g, p, dx, dp, R, H, c, stream);
+    }
+    if (H % 8 == 0 && aligned(x, 16) && aligned(g, 16) && aligned(dx, 16)) {
+        return b4 ? launch_bwd<true, Bwd16>(K_BWD16_B4, x, g, p, dx, dp, R, H, c, stream)
+                  : launch_bwd<false, Bwd16>(K_BWD16_GEN, x, g, p, dx, dp, R, H, c, stream);
     }
     const uint16_t* xs = (const uint16_t*)x;
     const uint16_t* gs = (const uint16_t*)g;
     uint16_t* dxs = (uint16_t*)dx;
-    if (b4) return launch(6, bwd_elem_kernel<true>, R, stream, xs, gs, p, dxs, dp, R, H, c);
-    return launch(7, bwd_elem_kernel<false>, R, stream, xs, gs, p, dxs, dp, R, H, c);
+    if (b4) return launch(K_BWDE_B4, bwd_elem_kernel<true>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
+    return launch(K_BWDE_GEN, bwd_elem_kernel<false>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
 }
 
 const char* situ_glu_status_string(int status) {

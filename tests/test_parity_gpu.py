@@ -154,11 +154,12 @@ def test_misaligned_bases_take_the_element_path(sg, H):
     par = Parity(f"misaligned H={H}")
     compare_full(par, x, g, p0, out, dx, dp)
     par.assert_ok()
-    # and the aligned vector path gives the same bits
+    # the aligned vector path gives the same bits elementwise; dp is summed in another order
+    # (per lane: strided elements here, 8-element chunks there), so it agrees to fp32 rounding
     out2, dx2, dp2 = run(sg, x0, g0, p0)
     assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
     assert torch.equal(dx.view(torch.int16), dx2.view(torch.int16))
-    assert torch.equal(dp, dp2)
+    torch.testing.assert_close(dp, dp2, rtol=1e-5, atol=1e-4)
 
 
 def test_extreme_and_nonfinite_inputs(sg):
