@@ -122,9 +122,11 @@ __device__ __forceinline__ float warp_sum(float v) {
 // Vector path. cpr = chunks of NW words per half-row (H = 2·NW·cpr); the launch shape S gives
 // NW, U (chunks per lane loaded before the math), TPB (threads per CTA) and MINB (resident
 // CTAs per SM requested from the register allocator).
-template <bool BETA4, class S, int NW = S::NW, int U = S::U, int TPB = S::TPB>
-__global__ void __launch_bounds__(S::TPB, S::MINB) fwd_vec_kernel(const Vec<NW>* __restrict__ x, Vec<NW>* __restrict__ out,
-                                                            int64_t R, int cpr, Coef c) {
+template <bool BETA4, class S>
+__global__ void __launch_bounds__(S::TPB, S::MINB) fwd_vec_kernel(const Vec<S::NW>* __restrict__ x,
+                                                                  Vec<S::NW>* __restrict__ out, int64_t R, int cpr,
+                                                                  Coef c) {
+    constexpr int NW = S::NW, U = S::U, TPB = S::TPB;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = ((int64_t)blockIdx.x * TPB + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * TPB) >> 5;
@@ -203,10 +205,11 @@ __device__ __forceinline__ void bwd_chunk(const Vec<NW>& gv, const Vec<NW>& lv, 
 // Vector path. dx may equal x (in place): every chunk of x is loaded by the lane that later
 // stores the same chunk of dx, and no thread reads a chunk after it was written, so x is
 // read through the coherent path.
-template <bool BETA4, class S, int NW = S::NW, int U = S::U, int TPB = S::TPB>
-__global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<NW>* x, const Vec<NW>* __restrict__ g,
-                                                            const float* __restrict__ p, Vec<NW>* dx,
-                                                            float* __restrict__ dp, int64_t R, int cpr, Coef c) {
+template <bool BETA4, class S>
+__global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<S::NW>* x, const Vec<S::NW>* __restrict__ g,
+                                                                  const float* __restrict__ p, Vec<S::NW>* dx,
+                                                                  float* __restrict__ dp, int64_t R, int cpr, Coef c) {
+    constexpr int NW = S::NW, U = S::U, TPB = S::TPB;
     const int lane = threadIdx.x & 31;
     const int64_t warp0 = ((int64_t)blockIdx.x * TPB + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * TPB) >> 5;

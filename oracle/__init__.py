@@ -35,6 +35,8 @@ _lib = None
 
 # The same flags on x86_64 and aarch64: no FMA contraction, no fast-math, so
 # both machines evaluate exactly the expressions written in the C file.
+FP8_BLOCK = 128  # elements per FP8 scale block (along a row, within each half)
+
 GCC_FLAGS = ["-O2", "-std=c11", "-fPIC", "-shared", "-ffp-contract=off", "-fno-fast-math"]
 
 
@@ -70,6 +72,14 @@ class Oracle:
         lib.oracle_situ_glu_fwd_bf16.restype = cint
         lib.oracle_situ_glu_bwd_router_bf16.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, dbl, dbl, cint]
         lib.oracle_situ_glu_bwd_router_bf16.restype = cint
+        lib.oracle_e4m3_encode.argtypes = [ctypes.c_float]
+        lib.oracle_e4m3_encode.restype = ctypes.c_uint8
+        lib.oracle_e4m3_decode.argtypes = [ctypes.c_uint8]
+        lib.oracle_e4m3_decode.restype = ctypes.c_float
+        lib.oracle_quantize_fp8.argtypes = [vp, vp, vp, i64, i64, i64]
+        lib.oracle_quantize_fp8.restype = cint
+        lib.oracle_dequantize_fp8.argtypes = [vp, vp, vp, i64, i64, i64]
+        lib.oracle_dequantize_fp8.restype = cint
         self.lib = lib
         self.path = path
 
@@ -137,6 +147,45 @@ class Oracle:
         return dx, dp, dpa
 
 
+    # ---------------- block-wise FP8 saved x ----------------
+
+    def e4m3_encode(self, v: float) -> int:
+        """OCP E4M3 code of fp32 v: round to nearest (ties to even code), saturate to +-448."""
+        return int(self.lib.oracle_e4m3_encode(float(v)))
+
+    def e4m3_decode(self, code: int) -> float:
+        return float(self.lib.oracle_e4m3_decode(int(code) & 0xFF))
+
+    def quantize_fp8(self, x_bits, block: int = FP8_BLOCK):
+        """bf16 bits x [R,2H] -> (codes uint8 [R,2H], scales fp32 [R, 2*ceil(H/block)])."""
+        x_bits = np.ascontiguousarray(x_bits).view(np.uint16)
+        R, H2 = x_bits.shape
+        H = H2 // 2
+        nb = -(-H // block)
+        q = np.empty((R, H2), dtype=np.uint8)
+        sc = np.empty((R, 2 * nb), dtype=np.float32)
+        _check(self.lib.oracle_quantize_fp8(_ptr(x_bits), _ptr(q), _ptr(sc), R, H, block))
+        return q, sc
+
+    def dequantize_fp8(self, q, sc, block: int = FP8_BLOCK):
+        """(codes [R,2H], scales [R,2nb]) -> x^ fp32 [R,2H] = decode(code) * scale."""
+        q = np.ascontiguousarray(q, dtype=np.uint8)
+        sc = np.ascontiguousarray(sc, dtype=np.float32)
+        R, H2 = q.shape
+        xh = np.empty((R, H2), dtype=np.float32)
+        _check(self.lib.oracle_dequantize_fp8(_ptr(q), _ptr(sc), _ptr(xh), R, H2 // 2, block))
+        return xh
+
+    def bwd_router_fp8(self, q, sc, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0,
+                       block: int = FP8_BLOCK):
+        """Backward with the router rewrite from the FP8-saved x: the definition evaluated on
+        x^ = decode(q) * s (fp32, widened exactly to double)."""
+        xh = self.dequantize_fp8(q, sc, block).astype(np.float64)
+        g = (np.ascontiguousarray(g_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32)
+        return self.bwd_router_f64(xh, g.astype(np.float64), np.asarray(p, dtype=np.float32).astype(np.float64),
+                                   beta, lbeta, nthreads)
+
+
 def _ptr(a: np.ndarray) -> int:
     return a.ctypes.data
 
@@ -194,3 +243,24 @@ def fwd_bf16(x_bits, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
 
 def bwd_router_bf16(x_bits, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
     return _default().bwd_router_bf16(x_bits, g_bits, p, beta, lbeta, nthreads)
+
+
+def e4m3_encode(v: float) -> int:
+    return _default().e4m3_encode(v)
+
+
+def e4m3_decode(code: int) -> float:
+    return _default().e4m3_decode(code)
+
+
+def quantize_fp8(x_bits, block: int = FP8_BLOCK):
+    return _default().quantize_fp8(x_bits, block)
+
+
+def dequantize_fp8(q, sc, block: int = FP8_BLOCK):
+    return _default().dequantize_fp8(q, sc, block)
+
+
+def bwd_router_fp8(q, sc, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0,
+                   block: int = FP8_BLOCK):
+    return _default().bwd_router_fp8(q, sc, g_bits, p, beta, lbeta, nthreads, block)

@@ -279,3 +279,97 @@ int oracle_situ_glu_bwd_router_bf16(const uint16_t* x, const uint16_t* g, const 
     jb.lbeta = lbeta;
     return run_rows(jb, R, nthreads);
 }
+
+/* ===================================================================================
+ * Block-wise FP8 saved x ([K3-MEM], section "统一激活管理器：重算、量化、offload 都是存储策略":
+ * most activations saved for backward are stored block-wise in FP8; elementwise operators
+ * recompute). The pages leave the format open; the readings taken here:
+ *   - FP8 E4M3 as defined by the OCP 8-bit floating point format (bias 7, 3 mantissa bits,
+ *     subnormals, largest finite 448, code 0x7F/0xFF is NaN, no infinity);
+ *   - blocks of 128 consecutive elements along a row, separately within the gate half and the
+ *     linear half (the last block of a half may be shorter); nb = ceil(H / 128) per half;
+ *   - one fp32 scale per block from the block's amax floored at 448 * 2^-126 (so the scale is a
+ *     normal fp32 and 448 / amax cannot overflow): a = max(amax, 448 * 2^-126), s = a / 448,
+ *     codes q = E4M3_RNE_satfinite(x * (448 / a)); dequantised x^ = decode(q) * s. An all-zero
+ *     block gets s = 2^-126 and codes 0.
+ * Every one of these steps is a single IEEE fp32 operation (amax exact, division and product
+ * rounded to nearest), so the integer codes are fixed by the definition itself.
+ * =================================================================================== */
+
+/* value of a non-negative E4M3 code 0x00..0x7E (exact in float) */
+static float e4m3_mag(int c) {
+    int e = (c >> 3) & 0xF, m = c & 7;
+    if (e == 0) return ldexpf((float)m, -9);           /* subnormal: m/8 * 2^-6 */
+    return ldexpf((float)(8 + m), e - 10);              /* (1 + m/8) * 2^(e-7) */
+}
+
+float oracle_e4m3_decode(uint8_t code) {
+    int c = code & 0x7F;
+    if (c == 0x7F) return NAN;
+    float v = e4m3_mag(c);
+    return (code & 0x80) ? -v : v;
+}
+
+/* Round to nearest E4M3 (ties to the even code), saturating finite values to +-448. */
+uint8_t oracle_e4m3_encode(float v) {
+    if (isnan(v)) return 0x7F;
+    uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    float a = fabsf(v);
+    if (a >= 448.0f) return sign | 0x7E;
+    /* largest code whose value is <= a (codes are monotone in value), by bisection */
+    int lo = 0, hi = 0x7E;
+    while (lo < hi) {
+        int mid = (lo + hi + 1) / 2;
+        if (e4m3_mag(mid) <= a) lo = mid; else hi = mid - 1;
+    }
+    int c = lo;
+    if (c < 0x7E) {
+        float below = e4m3_mag(c), above = e4m3_mag(c + 1);
+        float d_lo = a - below, d_hi = above - a;       /* exact: both sides are representable steps */
+        if (d_hi < d_lo || (d_hi == d_lo && (c & 1))) c = c + 1;
+    }
+    return (uint8_t)(sign | c);
+}
+
+/* One row half (n elements of bf16 bits) -> codes and scales of its blocks. */
+static void quantize_half(const uint16_t* xb, int64_t n, uint8_t* q, float* s, int64_t block) {
+    for (int64_t b0 = 0, bi = 0; b0 < n; b0 += block, ++bi) {
+        int64_t b1 = b0 + block < n ? b0 + block : n;
+        float amax = 0.0f;
+        for (int64_t j = b0; j < b1; ++j) {
+            float v = fabsf((float)oracle_bf16_to_double(xb[j]));
+            if (v > amax) amax = v;
+        }
+        const float floor_amax = 448.0f * 0x1p-126f;     /* exact: 7 * 2^-120 */
+        if (amax < floor_amax) amax = floor_amax;
+        s[bi] = amax / 448.0f;
+        float inv = 448.0f / amax;
+        for (int64_t j = b0; j < b1; ++j) q[j] = oracle_e4m3_encode((float)oracle_bf16_to_double(xb[j]) * inv);
+    }
+}
+
+/* x bf16 [R,2H] -> q uint8 [R,2H], s fp32 [R, 2*nb] (gate blocks, then linear blocks). */
+int oracle_quantize_fp8(const uint16_t* x, uint8_t* q, float* s, int64_t R, int64_t H, int64_t block) {
+    if (R < 0 || H <= 0 || block <= 0) return 1;
+    int64_t nb = (H + block - 1) / block;
+    for (int64_t r = 0; r < R; ++r) {
+        quantize_half(x + r * 2 * H, H, q + r * 2 * H, s + r * 2 * nb, block);
+        quantize_half(x + r * 2 * H + H, H, q + r * 2 * H + H, s + r * 2 * nb + nb, block);
+    }
+    return 0;
+}
+
+/* q, s -> x^ fp32 [R,2H] = decode(q) * s, one fp32 product per element. */
+int oracle_dequantize_fp8(const uint8_t* q, const float* s, float* xhat, int64_t R, int64_t H, int64_t block) {
+    if (R < 0 || H <= 0 || block <= 0) return 1;
+    int64_t nb = (H + block - 1) / block;
+    for (int64_t r = 0; r < R; ++r) {
+        for (int64_t half = 0; half < 2; ++half) {
+            for (int64_t j = 0; j < H; ++j) {
+                float sc = s[r * 2 * nb + half * nb + j / block];
+                xhat[r * 2 * H + half * H + j] = oracle_e4m3_decode(q[r * 2 * H + half * H + j]) * sc;
+            }
+        }
+    }
+    return 0;
+}

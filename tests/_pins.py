@@ -291,3 +291,124 @@ def pin_empty_rows(o):
     assert out.shape == (0, 4)
     dx, dp, dpa = o.bwd_router_f64(np.zeros((0, 8)), np.zeros((0, 4)), np.zeros((0,)))
     assert dx.shape == (0, 8) and dp.shape == (0,)
+
+
+# ---------------------------------------------------------------- block-wise FP8 saved x
+
+def _e4m3_table():
+    """Values of the non-negative finite E4M3 codes 0x00..0x7E from the OCP 8-bit floating point
+    format definition: exponent field e (bias 7), mantissa m/8, subnormals at e = 0."""
+    vals = []
+    for c in range(0x7F):
+        e, m = c >> 3, c & 7
+        vals.append(m / 8 * 2.0 ** -6 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7))
+    return vals
+
+
+def _brute_e4m3(v: float) -> int:
+    """Nearest code by exhaustive search over all finite codes, ties to the even code,
+    saturating beyond the largest finite value (an implementation independent of the oracle's)."""
+    if math.isnan(v):
+        return 0x7F
+    sign = 0x80 if math.copysign(1.0, v) < 0 else 0
+    a = abs(v)
+    vals = _e4m3_table()
+    if a >= vals[-1]:
+        return sign | 0x7E
+    best = min(range(len(vals)), key=lambda c: (abs(vals[c] - a), c & 1))
+    return sign | best
+
+
+def pin_e4m3_codec(o):
+    vals = _e4m3_table()
+    assert vals[0x7E] == 448.0 and vals[0x01] == 2.0 ** -9 and vals[0x08] == 2.0 ** -6 and vals[0x38] == 1.0
+    for c in range(0x7F):                                   # exact round trip of every finite code
+        assert o.e4m3_decode(c) == vals[c] and o.e4m3_decode(c | 0x80) == -vals[c]
+        assert o.e4m3_encode(vals[c]) == c and o.e4m3_encode(-vals[c]) == (c | 0x80 if c else 0x80)
+    assert math.isnan(o.e4m3_decode(0x7F)) and math.isnan(o.e4m3_decode(0xFF))
+    probes = [0.0, 448.0, 449.0, 464.0, 479.0, 1e6, 3e38, 2.0 ** -10, 2.0 ** -11, 1e-30]
+    for c in range(0x7E):                                    # every midpoint and its fp32 neighbours
+        mid = (vals[c] + vals[c + 1]) / 2
+        probes += [mid, float(np.nextafter(np.float32(mid), np.float32(0))),
+                   float(np.nextafter(np.float32(mid), np.float32(1e9)))]
+    rng = np.random.default_rng(8)
+    probes += list(np.exp2(rng.uniform(-12, 9.5, 400)).astype(np.float32))
+    for v in probes:
+        v = float(np.float32(v))
+        for s in (v, -v):
+            assert o.e4m3_encode(s) == _brute_e4m3(s), (s, o.e4m3_encode(s), _brute_e4m3(s))
+    assert o.e4m3_encode(float("nan")) & 0x7F == 0x7F
+    # PyTorch's float8_e4m3fn cast (round to nearest even) agrees inside the finite range
+    inrange = torch.tensor([p for p in probes if abs(p) <= 448.0], dtype=torch.float32)
+    tq = inrange.to(torch.float8_e4m3fn).view(torch.uint8).tolist()
+    assert tq == [o.e4m3_encode(float(p)) for p in inrange.tolist()]
+
+
+def _bf16_bits(a: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+
+def _bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+def pin_fp8_block_quantization(o):
+    rng = np.random.default_rng(4)
+    for H in (256, 200, 1):                                  # whole blocks, a short last block, H = 1
+        R, blk = 5, 128
+        nb = -(-H // blk)
+        x = rng.normal(0, 3, (R, 2 * H)).astype(np.float32)
+        x[1, :min(H, blk)] = 0.0                             # an all-zero gate block
+        x[2, H] = 1e30                                       # a huge value in the first linear block
+        x[3, :] *= 1e-38                                     # tiny values (subnormal codes)
+        xb = _bf16_bits(x)
+        xf = _bits_to_f32(xb)
+        q, sc = o.quantize_fp8(xb, blk)
+        xh = o.dequantize_fp8(q, sc, blk)
+        assert q.shape == (R, 2 * H) and sc.shape == (R, 2 * nb)
+        for r in range(R):
+            for half in range(2):
+                for b in range(nb):
+                    lo, hi = half * H + b * blk, half * H + min(H, (b + 1) * blk)
+                    blkv = xf[r, lo:hi]
+                    amax = np.float32(np.max(np.abs(blkv)))
+                    s = sc[r, half * nb + b]
+                    floor = np.float32(448.0 * 2.0 ** -126)
+                    assert s == np.float32(max(amax, floor) / np.float32(448.0))
+                    if amax == 0:
+                        assert np.all(q[r, lo:hi] == 0) and np.all(xh[r, lo:hi] == 0)
+                        continue
+                    if amax >= floor:                                   # the amax element saturates the range
+                        assert (q[r, lo:hi][np.argmax(np.abs(blkv))] & 0x7F) == 0x7E
+                    # half an E4M3 step: 2^-4 relative for normal codes, 2^-10·s absolute for subnormal
+                    # codes; plus the fp32 rounding of the products and of a subnormal fp32 result
+                    err = np.abs(xh[r, lo:hi].astype(np.float64) - blkv.astype(np.float64))
+                    bound = np.maximum(2.0 ** -4 * np.abs(blkv), 2.0 ** -10 * float(s)) * (1 + 2 ** -20) \
+                        + 2.0 ** -23 * np.abs(blkv) + 2.0 ** -149
+                    assert np.all(err <= bound), (H, r, half, b, float(err.max()))
+        # locality: changing one element only changes its own block
+        x2 = x.copy()
+        x2[0, H + (H - 1)] = 77.0
+        q2, sc2 = o.quantize_fp8(_bf16_bits(x2), blk)
+        changed = np.nonzero(sc2 != sc)
+        assert set(zip(*changed)) <= {(0, nb + (H - 1) // blk)}
+        assert np.array_equal(q2[1:], q[1:]) and np.array_equal(q2[0, :H], q[0, :H])
+    # dequantisation uses the scale of the element's own half and block
+    q = np.full((1, 2 * 256), 0x38, dtype=np.uint8)          # every code = 1.0
+    sc = np.array([[1.0, 2.0, 4.0, 8.0]], dtype=np.float32)
+    xh = o.dequantize_fp8(q, sc, 128)
+    assert np.array_equal(xh[0], np.repeat(np.array([1.0, 2.0, 4.0, 8.0], dtype=np.float32), 128))
+
+
+def pin_fp8_backward_is_backward_of_dequantized(o):
+    """The FP8 backward is the bf16 backward evaluated on the dequantised x (exactly)."""
+    rng = np.random.default_rng(9)
+    R, H = 3, 200
+    xb = _bf16_bits(rng.normal(0, 3, (R, 2 * H)))
+    gb = _bf16_bits(rng.normal(0, 1, (R, H)))
+    p = rng.uniform(0, 1, R).astype(np.float32)
+    q, sc = o.quantize_fp8(xb)
+    dx, dp, dpa = o.bwd_router_fp8(q, sc, gb, p)
+    xh = o.dequantize_fp8(q, sc).astype(np.float64)
+    dx2, dp2, _ = o.bwd_router_f64(xh, _bits_to_f32(gb).astype(np.float64), p.astype(np.float64))
+    assert np.array_equal(dx, dx2) and np.array_equal(dp, dp2)

@@ -24,6 +24,9 @@ PINS = [
     ("autograd", lambda o: _pins.pin_autograd_of_definition(o, 4.0, 25.0)),
     ("bf16_vs_f64", _pins.pin_bf16_entry_matches_f64_entry),
     ("extreme", _pins.pin_extreme_finite_inputs),
+    ("e4m3_codec", _pins.pin_e4m3_codec),
+    ("fp8_blocks", _pins.pin_fp8_block_quantization),
+    ("fp8_bwd", _pins.pin_fp8_backward_is_backward_of_dequantized),
 ]
 
 MUTANTS = {
@@ -49,6 +52,17 @@ MUTANTS = {
     "bf16_p_index_wrong": ("p = (double)((const float*)jb->p)[r];", "p = (double)((const float*)jb->p)[0];"),
     "g_row_off_by_one": ("gr = (const double*)jb->g + r * H;",
                          "gr = (const double*)jb->g + (r > 0 ? r - 1 : 0) * H;"),
+    # block-wise FP8 saved x
+    "e4m3_ties_not_to_even": ("if (d_hi < d_lo || (d_hi == d_lo && (c & 1))) c = c + 1;",
+                              "if (d_hi <= d_lo) c = c + 1;"),
+    "e4m3_overflow_to_nan": ("if (a >= 448.0f) return sign | 0x7E;", "if (a >= 448.0f) return sign | 0x7F;"),
+    "e4m3_subnormal_scale": ("if (e == 0) return ldexpf((float)m, -9);", "if (e == 0) return ldexpf((float)m, -10);"),
+    "e4m3_bias": ("return ldexpf((float)(8 + m), e - 10);", "return ldexpf((float)(8 + m), e - 9);"),
+    "fp8_scale_divisor": ("s[bi] = amax / 448.0f;", "s[bi] = amax / 256.0f;"),
+    "fp8_no_amax_floor": ("if (amax < floor_amax) amax = floor_amax;", "(void)floor_amax;"),
+    "fp8_linear_scales_overwrite_gate": ("s + r * 2 * nb + nb, block);", "s + r * 2 * nb, block);"),
+    "fp8_dequant_ignores_half": ("float sc = s[r * 2 * nb + half * nb + j / block];",
+                                 "float sc = s[r * 2 * nb + j / block];"),
 }
 
 

@@ -76,3 +76,15 @@ def test_extreme_finite_inputs_give_finite_outputs():
 
 def test_empty_rows_ok():
     _pins.pin_empty_rows(oracle)
+
+
+def test_e4m3_codec():
+    _pins.pin_e4m3_codec(oracle)
+
+
+def test_fp8_block_quantization():
+    _pins.pin_fp8_block_quantization(oracle)
+
+
+def test_fp8_backward_is_backward_of_dequantized():
+    _pins.pin_fp8_backward_is_backward_of_dequantized(oracle)
