@@ -63,6 +63,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 saved-x variant's timing")
     ap.add_argument("--rows", type=int, default=None, help="override R (for small profiling runs)")
     return ap.parse_args(argv)
 
@@ -338,6 +339,8 @@ def run_native(args):
     bwd_gbs = bwd_bytes / (bwd_avg * 1e-3) / 1e9
     step_gbs = (fwd_bytes + bwd_bytes) / (elapsed_ms / K * 1e-3) / 1e9
 
+    fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
+
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_hash() and NCU_TRAFFIC["bwd_bytes_per_row"]:
         traffic = NCU_TRAFFIC["bwd_bytes_per_row"] * R
@@ -389,12 +392,55 @@ def run_native(args):
         "gpu_launches": 2 * K,
         "e2e": e2e,
         "cpu_baseline": cpu,
+        "fp8_saved_x": fp8,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
     return 0
+
+
+def time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, warmup, peak):
+    """The block-wise FP8 saved-x variant on the same workload: forward that also writes the
+    E4M3 codes and block scales of x, backward + router gradient from them."""
+    import torch
+    nb = sg.fp8_scale_blocks(H)
+    xq = torch.empty((R, 2 * H), dtype=torch.uint8, device=dev)
+    xs = torch.empty((R, 2 * nb), dtype=torch.float32, device=dev)
+    sh = int(stream.cuda_stream)
+    lib = sg.load()
+
+    def fwd():
+        sg._check(lib.situ_glu_fwd_save_fp8(x.data_ptr(), out.data_ptr(), xq.data_ptr(), xs.data_ptr(), R, H,
+                                            4.0, 25.0, sh))
+
+    def bwd():
+        sg._check(lib.situ_glu_bwd_router_fp8(xq.data_ptr(), xs.data_ptr(), g.data_ptr(), p.data_ptr(),
+                                              dx.data_ptr(), dp.data_ptr(), R, H, 4.0, 25.0, sh))
+
+    for _ in range(max(1, warmup)):
+        fwd()
+        bwd()
+    torch.cuda.synchronize(dev)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    for i in range(steps):
+        ev[i][0].record(stream)
+        fwd()
+        ev[i][1].record(stream)
+        bwd()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize(dev)
+    f_ms = sum(e[0].elapsed_time(e[1]) for e in ev) / steps
+    b_ms = sum(e[1].elapsed_time(e[2]) for e in ev) / steps
+    fb = (8 * H + 8 * nb) * R
+    bb = (8 * H + 8 * nb + 8) * R
+    del xq, xs
+    return {"fwd_save_fp8": {"ms": f_ms, "GB_s": fb / f_ms / 1e6, "frac_of_peak": fb / f_ms / 1e6 / peak, "bytes": fb},
+            "bwd_router_fp8": {"ms": b_ms, "GB_s": bb / b_ms / 1e6, "frac_of_peak": bb / b_ms / 1e6 / peak, "bytes": bb},
+            "rows_per_s": R / ((f_ms + b_ms) * 1e-3),
+            "saved_bytes_per_row": {"bf16_x": 4 * H, "fp8_x": 2 * H + 8 * nb},
+            "gpu_launches": 2 * steps}
 
 
 def pinned_like(t):

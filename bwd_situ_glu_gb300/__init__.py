@@ -28,8 +28,9 @@ CSRC = os.path.join(_HERE, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
-SOURCES = [os.path.join(CSRC, "situ_glu.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, "situ_math.cuh"), os.path.join(INCLUDE, "situ_glu.h")]
+SOURCES = [os.path.join(CSRC, "situ_glu.cu"), os.path.join(CSRC, "situ_glu_fp8.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h")] + [
+    os.path.join(INCLUDE, "situ_glu.h")]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
@@ -83,6 +84,10 @@ def load():
     lib.situ_glu_fwd.restype = cint
     lib.situ_glu_bwd_router.argtypes = [vp, vp, vp, vp, vp, i64, i64, f32, f32, vp]
     lib.situ_glu_bwd_router.restype = cint
+    lib.situ_glu_fwd_save_fp8.argtypes = [vp, vp, vp, vp, i64, i64, f32, f32, vp]
+    lib.situ_glu_fwd_save_fp8.restype = cint
+    lib.situ_glu_bwd_router_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, f32, vp]
+    lib.situ_glu_bwd_router_fp8.restype = cint
     lib.situ_glu_status_string.argtypes = [cint]
     lib.situ_glu_status_string.restype = ctypes.c_char_p
     lib.situ_glu_last_cuda_error.argtypes = []
@@ -184,8 +189,66 @@ def situ_glu_bwd_router(x, g, p, dx=None, dp=None, beta: float = 4.0, lbeta: flo
     return dx, dp
 
 
+FP8_BLOCK = 128  # elements per FP8 scale block (SITU_GLU_FP8_BLOCK)
+
+
+def fp8_scale_blocks(H: int) -> int:
+    return -(-H // FP8_BLOCK)
+
+
+def situ_glu_fwd_save_fp8(x, out=None, xq=None, xs=None, beta: float = 4.0, lbeta: float = 25.0, stream=None):
+    """(out bf16 [R,H], xq uint8 [R,2H], xs fp32 [R,2*nb]): the forward plus x saved in block-wise FP8."""
+    import torch
+    if x.dim() != 2 or x.shape[1] % 2 != 0:
+        raise ValueError("x must be [R, 2H]")
+    R, H = x.shape[0], x.shape[1] // 2
+    nb = fp8_scale_blocks(H)
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    if out is None:
+        out = torch.empty((R, H), dtype=torch.bfloat16, device=x.device)
+    if xq is None:
+        xq = torch.empty((R, 2 * H), dtype=torch.uint8, device=x.device)
+    if xs is None:
+        xs = torch.empty((R, 2 * nb), dtype=torch.float32, device=x.device)
+    _need(out, torch.bfloat16, (R, H), "out")
+    _need(xq, torch.uint8, (R, 2 * H), "xq")
+    _need(xs, torch.float32, (R, 2 * nb), "xs")
+    if len({t.device for t in (x, out, xq, xs)}) != 1:
+        raise ValueError("all tensors must be on the same device")
+    with torch.cuda.device(x.device):
+        _check(load().situ_glu_fwd_save_fp8(x.data_ptr(), out.data_ptr(), xq.data_ptr(), xs.data_ptr(), R, H,
+                                            beta, lbeta, _stream_handle(stream, x.device)))
+    return out, xq, xs
+
+
+def situ_glu_bwd_router_fp8(xq, xs, g, p, dx=None, dp=None, beta: float = 4.0, lbeta: float = 25.0, stream=None):
+    """(dx bf16 [R,2H], dp fp32 [R]) of the fused backward + router gradient from the FP8-saved x."""
+    import torch
+    if xq.dim() != 2 or xq.shape[1] % 2 != 0:
+        raise ValueError("xq must be [R, 2H]")
+    R, H = xq.shape[0], xq.shape[1] // 2
+    nb = fp8_scale_blocks(H)
+    _need(xq, torch.uint8, (R, 2 * H), "xq")
+    _need(xs, torch.float32, (R, 2 * nb), "xs")
+    _need(g, torch.bfloat16, (R, H), "g")
+    _need(p, torch.float32, (R,), "p")
+    if dx is None:
+        dx = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=xq.device)
+    if dp is None:
+        dp = torch.empty((R,), dtype=torch.float32, device=xq.device)
+    _need(dx, torch.bfloat16, (R, 2 * H), "dx")
+    _need(dp, torch.float32, (R,), "dp")
+    if len({t.device for t in (xq, xs, g, p, dx, dp)}) != 1:
+        raise ValueError("all tensors must be on the same device")
+    with torch.cuda.device(xq.device):
+        _check(load().situ_glu_bwd_router_fp8(xq.data_ptr(), xs.data_ptr(), g.data_ptr(), p.data_ptr(), dx.data_ptr(),
+                                              dp.data_ptr(), R, H, beta, lbeta, _stream_handle(stream, xq.device)))
+    return dx, dp
+
+
 __all__ = [
     "build", "load", "version", "status_string", "SituGluError",
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
+    "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
     "LIB_PATH", "INCLUDE",
 ]

@@ -23,97 +23,15 @@
 #include <math.h>
 #include <stdint.h>
 
-#include <mutex>
-
 #include "../../include/situ_glu.h"
+#include "situ_device.cuh"
+#include "situ_host.h"
 #include "situ_math.cuh"
 
 namespace {
 
-using situ::Coef;
-
-// ---------------------------------------------------------------------------
-// memory helpers (inline PTX)
-// ---------------------------------------------------------------------------
-
-// NW consecutive 32-bit words (2·NW bf16): NW = 4 is a 16-byte chunk, NW = 8 a 32-byte chunk.
-template <int NW>
-struct Vec {
-    uint32_t w[NW];
-};
-
-// Streaming load. NC = true reads through the non-coherent path (inputs no thread writes);
-// NC = false through the coherent path (x, which dx may alias in place). NOALLOC adds the
-// L1::no_allocate hint (measured faster for the 32-byte backward, slower for the 16-byte one).
-template <int NW, bool NC, bool NOALLOC = true>
-__device__ __forceinline__ Vec<NW> ld_stream(const Vec<NW>* p) {
-    Vec<NW> v;
-    if constexpr (NW == 4) {
-        if constexpr (NC && NOALLOC)
-            asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                : "l"(p));
-        else if constexpr (NC)
-            asm("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                : "l"(p));
-        else if constexpr (NOALLOC)
-            asm("ld.global.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                : "l"(p));
-        else
-            asm("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
-                : "l"(p));
-    } else {
-        static_assert(NW == 8, "16- or 32-byte vectors");
-        static_assert(NOALLOC, "the 32-byte path always uses L1::no_allocate");
-        if constexpr (NC)
-            asm("ld.global.nc.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
-                  "=r"(v.w[6]), "=r"(v.w[7])
-                : "l"(p));
-        else
-            asm("ld.global.L1::no_allocate.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
-                : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3]), "=r"(v.w[4]), "=r"(v.w[5]),
-                  "=r"(v.w[6]), "=r"(v.w[7])
-                : "l"(p));
-    }
-    return v;
-}
-
-// Streaming (evict-first) store.
-template <int NW>
-__device__ __forceinline__ void st_stream(Vec<NW>* p, const Vec<NW>& v) {
-    if constexpr (NW == 4) {
-        asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]), "r"(v.w[2]),
-                     "r"(v.w[3])
-                     : "memory");
-    } else {
-        asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(v.w[0]), "r"(v.w[1]),
-                     "r"(v.w[2]), "r"(v.w[3]), "r"(v.w[4]), "r"(v.w[5]), "r"(v.w[6]), "r"(v.w[7])
-                     : "memory");
-    }
-}
-
-__device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-__device__ __forceinline__ float bf16_to_f32(uint16_t b) { return __uint_as_float(((uint32_t)b) << 16); }
-
-// Two fp32 -> packed bf16x2 (round to nearest even); lo goes to the low half.
-__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
-    uint32_t r;
-    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
-    return r;
-}
-
-__device__ __forceinline__ uint16_t f32_to_bf16(float f) { return (uint16_t)(pack_bf16x2(f, 0.0f) & 0xFFFFu); }
-
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
-}
+using namespace situ;
+using namespace situ_host;
 
 // ---------------------------------------------------------------------------
 // forward kernels
@@ -195,8 +113,8 @@ __device__ __forceinline__ void bwd_chunk(const Vec<NW>& gv, const Vec<NW>& lv, 
         float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
         situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gv.w[i]), bf16_lo(lv.w[i]), p * g0, c);
         situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gv.w[i]), bf16_hi(lv.w[i]), p * g1, c);
-        acc = fmaf(g0, b0.a, acc);
-        acc = fmaf(g1, b1.a, acc);
+        acc = fmaf(g0, b0.a16, acc);
+        acc = fmaf(g1, b1.a16, acc);
         dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
         dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
     }
@@ -219,7 +137,7 @@ __global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<S::N
         const Vec<NW>* gr = g + r * (int64_t)cpr;
         Vec<NW>* dgr = dx + r * (2 * (int64_t)cpr);
         Vec<NW>* dlr = dgr + cpr;
-        const float pr = p[r];
+        const float pr = 16.0f * p[r];   // 16·p: see situ::Bwd
         float acc = 0.0f;
         for (int c0 = 0; c0 < cpr; c0 += 32 * U) {
             Vec<NW> gv[U], lv[U], yv[U];
@@ -244,7 +162,7 @@ __global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<S::N
             }
         }
         acc = warp_sum(acc);
-        if (lane == 0) dp[r] = acc;
+        if (lane == 0) dp[r] = 16.0f * acc;
     }
 }
 
@@ -262,19 +180,19 @@ __global__ void __launch_bounds__(kElemThreads) bwd_elem_kernel(const uint16_t* 
         const uint16_t* xr = x + r * 2 * H;
         const uint16_t* gr = g + r * H;
         uint16_t* dxr = dx + r * 2 * H;
-        const float pr = p[r];
+        const float pr = 16.0f * p[r];   // 16·p: see situ::Bwd
         float acc = 0.0f;
         for (int64_t j = lane; j < H; j += 32) {
             float u = bf16_to_f32(xr[j]);
             float v = bf16_to_f32(xr[H + j]);
             float gj = bf16_to_f32(gr[j]);
             situ::Bwd b = situ::bwd<BETA4>(u, v, pr * gj, c);
-            acc = fmaf(gj, b.a, acc);
+            acc = fmaf(gj, b.a16, acc);
             dxr[j] = f32_to_bf16(b.dgate);
             dxr[H + j] = f32_to_bf16(b.dlin);
         }
         acc = warp_sum(acc);
-        if (lane == 0) dp[r] = acc;
+        if (lane == 0) dp[r] = 16.0f * acc;
     }
 }
 
@@ -303,121 +221,17 @@ struct Bwd16 {       // other H % 8 == 0
     static constexpr bool NOALLOC = false;
 };
 
-enum KernelId {
-    K_FWD16BIG_B4, K_FWD16BIG_GEN, K_FWD16_B4, K_FWD16_GEN, K_FWDE_B4, K_FWDE_GEN,
-    K_BWD32_B4, K_BWD32_GEN, K_BWD16_B4, K_BWD16_GEN, K_BWDE_B4, K_BWDE_GEN,
-    K_COUNT
-};
-
-thread_local int t_last_cuda_error = 0;
-
-int cuda_fail(cudaError_t e) {
-    t_last_cuda_error = (int)e;
-    return SITU_GLU_CUDA_ERROR;
-}
-
-Coef make_coef(float beta, float lbeta) {
-    const double log2e = 1.4426950408889634074;
-    Coef c;
-    c.k_tu = (float)(-(2.0 / (double)beta) * log2e);
-    c.k_su = (float)(-log2e);
-    c.k_tv = (float)(-(2.0 / (double)lbeta) * log2e);
-    c.inv_beta = (float)(1.0 / (double)beta);
-    c.inv_lbeta = (float)(1.0 / (double)lbeta);
-    c.beta = beta;
-    c.lbeta = lbeta;
-    c.beta_lbeta = (float)((double)beta * (double)lbeta);
-    return c;
-}
-
-bool finite_positive(float f) { return isfinite(f) && f > 0.0f; }
-
-// The beta == 4 kernels share one exponential between tanh(u/4) and sigmoid(u) and skip the
-// small-argument series; their absolute error in L grows like lbeta * 2^-21, so they are used
-// only for lbeta <= 64 (error below 3e-5). Every other (beta, lbeta) takes the general kernels.
-constexpr float kFastMaxLbeta = 64.0f;
-bool fast_path(float beta, float lbeta) { return beta == 4.0f && lbeta <= kFastMaxLbeta; }
-
-struct Range {
-    uintptr_t lo, hi;  // [lo, hi)
-};
-
-bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
-
-Range range_of(const void* p, int64_t bytes) {
-    uintptr_t lo = (uintptr_t)p;
-    return Range{lo, lo + (uintptr_t)bytes};
-}
-
-bool aligned(const void* p, uintptr_t a) { return ((uintptr_t)p % a) == 0; }
-
-// Shared checks of R, H, beta, lbeta.
-int check_shape(int64_t R, int64_t H, float beta, float lbeta) {
-    if (R < 0 || H <= 0 || H > SITU_GLU_MAX_H) return SITU_GLU_INVALID_ARG;
-    if (!finite_positive(beta) || !finite_positive(lbeta)) return SITU_GLU_INVALID_ARG;
-    // R * 2H * 2 bytes must fit in int64
-    if (R > 0 && R > (INT64_MAX / 4) / H) return SITU_GLU_INVALID_ARG;
-    return SITU_GLU_OK;
-}
-
-// Per-device launch configuration cache: SM count and resident CTAs per SM for each kernel.
-constexpr int kMaxDevices = 64;
-std::mutex g_cfg_mutex;
-int g_sm_count[kMaxDevices];
-int g_blocks_per_sm[kMaxDevices][K_COUNT];
-
-int grid_for(int kernel_id, const void* fn, int tpb, int64_t R, int* grid) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e);
-    if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice);
-    int sms, per_sm;
-    {
-        std::lock_guard<std::mutex> lock(g_cfg_mutex);
-        if (g_sm_count[dev] == 0) {
-            int n = 0;
-            e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-            if (e != cudaSuccess) return cuda_fail(e);
-            g_sm_count[dev] = n;
-        }
-        if (g_blocks_per_sm[dev][kernel_id] == 0) {
-            int b = 0;
-            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&b, fn, tpb, 0);
-            if (e != cudaSuccess) return cuda_fail(e);
-            g_blocks_per_sm[dev][kernel_id] = b > 0 ? b : 1;
-        }
-        sms = g_sm_count[dev];
-        per_sm = g_blocks_per_sm[dev][kernel_id];
-    }
-    const int64_t persistent = (int64_t)sms * per_sm;
-    const int64_t warps_per_cta = tpb / 32;
-    const int64_t needed = (R + warps_per_cta - 1) / warps_per_cta;  // one warp per row
-    *grid = (int)(needed < persistent ? needed : persistent);
-    return SITU_GLU_OK;
-}
-
-template <typename Kernel, typename... Args>
-int launch(int kernel_id, Kernel kernel, int tpb, int64_t R, cudaStream_t stream, Args... args) {
-    int grid = 0;
-    int st = grid_for(kernel_id, (const void*)kernel, tpb, R, &grid);
-    if (st != SITU_GLU_OK) return st;
-    kernel<<<grid, tpb, 0, stream>>>(args...);
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e);
-    return SITU_GLU_OK;
-}
-
 template <bool B4, class S>
-int launch_fwd(int id, const void* x, void* out, int64_t R, int64_t H, const Coef& c, cudaStream_t stream) {
+int launch_fwd(const void* x, void* out, int64_t R, int64_t H, const Coef& c, cudaStream_t stream) {
     const int cpr = (int)(H / (2 * S::NW));
-    return launch(id, fwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (Vec<S::NW>*)out, R, cpr, c);
+    return launch(fwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (Vec<S::NW>*)out, R, cpr, c);
 }
 
 template <bool B4, class S>
-int launch_bwd(int id, const void* x, const void* g, const float* p, void* dx, float* dp, int64_t R, int64_t H,
+int launch_bwd(const void* x, const void* g, const float* p, void* dx, float* dp, int64_t R, int64_t H,
                const Coef& c, cudaStream_t stream) {
     const int cpr = (int)(H / (2 * S::NW));
-    return launch(id, bwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (const Vec<S::NW>*)g, p,
+    return launch(bwd_vec_kernel<B4, S>, S::TPB, R, stream, (const Vec<S::NW>*)x, (const Vec<S::NW>*)g, p,
                   (Vec<S::NW>*)dx, dp, R, cpr, c);
 }
 
@@ -438,15 +252,15 @@ int situ_glu_fwd(const void* x, void* out, int64_t R, int64_t H, float beta, flo
     const bool b4 = fast_path(beta, lbeta);
     if (H % 8 == 0 && aligned(x, 16) && aligned(out, 16)) {
         if (H % 512 == 0)
-            return b4 ? launch_fwd<true, Fwd16Big>(K_FWD16BIG_B4, x, out, R, H, c, stream)
-                      : launch_fwd<false, Fwd16Big>(K_FWD16BIG_GEN, x, out, R, H, c, stream);
-        return b4 ? launch_fwd<true, Fwd16>(K_FWD16_B4, x, out, R, H, c, stream)
-                  : launch_fwd<false, Fwd16>(K_FWD16_GEN, x, out, R, H, c, stream);
+            return b4 ? launch_fwd<true, Fwd16Big>(x, out, R, H, c, stream)
+                      : launch_fwd<false, Fwd16Big>(x, out, R, H, c, stream);
+        return b4 ? launch_fwd<true, Fwd16>(x, out, R, H, c, stream)
+                  : launch_fwd<false, Fwd16>(x, out, R, H, c, stream);
     }
     const uint16_t* xs = (const uint16_t*)x;
     uint16_t* os = (uint16_t*)out;
-    if (b4) return launch(K_FWDE_B4, fwd_elem_kernel<true>, kElemThreads, R, stream, xs, os, R, H, c);
-    return launch(K_FWDE_GEN, fwd_elem_kernel<false>, kElemThreads, R, stream, xs, os, R, H, c);
+    if (b4) return launch(fwd_elem_kernel<true>, kElemThreads, R, stream, xs, os, R, H, c);
+    return launch(fwd_elem_kernel<false>, kElemThreads, R, stream, xs, os, R, H, c);
 }
 
 int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, float* dp, int64_t R, int64_t H,
@@ -467,18 +281,18 @@ int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
     if (H % 16 == 0 && aligned(x, 32) && aligned(g, 32) && aligned(dx, 32)) {
-        return b4 ? launch_bwd<true, Bwd32>(K_BWD32_B4, x, g, p, dx, dp, R, H, c, stream)
-                  : launch_bwd<false, Bwd32>(K_BWD32_GEN, x, g, p, dx, dp, R, H, c, stream);
+        return b4 ? launch_bwd<true, Bwd32>(x, g, p, dx, dp, R, H, c, stream)
+                  : launch_bwd<false, Bwd32>(x, g, p, dx, dp, R, H, c, stream);
     }
     if (H % 8 == 0 && aligned(x, 16) && aligned(g, 16) && aligned(dx, 16)) {
-        return b4 ? launch_bwd<true, Bwd16>(K_BWD16_B4, x, g, p, dx, dp, R, H, c, stream)
-                  : launch_bwd<false, Bwd16>(K_BWD16_GEN, x, g, p, dx, dp, R, H, c, stream);
+        return b4 ? launch_bwd<true, Bwd16>(x, g, p, dx, dp, R, H, c, stream)
+                  : launch_bwd<false, Bwd16>(x, g, p, dx, dp, R, H, c, stream);
     }
     const uint16_t* xs = (const uint16_t*)x;
     const uint16_t* gs = (const uint16_t*)g;
     uint16_t* dxs = (uint16_t*)dx;
-    if (b4) return launch(K_BWDE_B4, bwd_elem_kernel<true>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
-    return launch(K_BWDE_GEN, bwd_elem_kernel<false>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
+    if (b4) return launch(bwd_elem_kernel<true>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
+    return launch(bwd_elem_kernel<false>, kElemThreads, R, stream, xs, gs, p, dxs, dp, R, H, c);
 }
 
 const char* situ_glu_status_string(int status) {

@@ -20,13 +20,19 @@
 // For β = 4, E1 = e^{−|u|/2} and E2 = E1², so one exponential serves the gate:
 // 2 ex2 + 1 rcp on the MUFU per element pair, forward and backward alike.
 //
-// Accuracy: ex2.approx and rcp.approx are within a few fp32 ulp (PTX ISA), so
-// every quantity above has a relative error of a few 2^-23, except (1 − E1)
-// and (1 − e) for tiny arguments, whose error is absolute (~2^-22). On the
-// β = 4 fast path that leaves an absolute error below λ·2^-21 in L and below
-// 2^-20 in G: tiny against the bf16 half-ulp or the 1e-3 floor of the outputs.
-// The general path replaces (1 − E1) and (1 − e) by a short odd Taylor series
-// of tanh below |z| < 1/16 so it stays relatively accurate for any β and λ.
+// Accuracy: ex2.approx and rcp.approx are within a few fp32 ulp (PTX ISA), so every quantity
+// above has a relative error of a few 2^-23, except the numerators 1 - E1 and 1 - e for small
+// arguments: E = ex2(t) carries an absolute error ~2^-22.5 near t = 0, so 1 - E computed as a
+// difference has a relative error ~2^-22.5 / |t|. The backward (whose dp has a purely relative
+// tolerance) therefore evaluates 1 - 2^t for t in (-0.0144, 0] by the exponential series
+// -t·ln2·(1 + t·ln2/2) (truncation below 1.7e-5 relative there; the difference form is better
+// than 1.7e-5 beyond), and the general path uses an odd Taylor series of tanh below |z| < 1/16.
+// The beta = 4 forward keeps the plain difference: its absolute error (below 2^-20 in G and
+// lbeta·2^-21 in L) is far inside the 1e-3 absolute floor of a bf16 output.
+//
+// The backward returns a/16, p·g·L·G' and p·g·G·L' from pg16 = 16·p·g: the factors 4 of G, G'
+// and L' (and 1/4 of L) are folded into the caller's per-row 16·p and the final 16·dp, exact
+// power-of-two scalings that save three multiplies per element pair.
 #pragma once
 
 #include <stdint.h>
@@ -43,6 +49,8 @@ struct Coef {
     float beta;      // β
     float lbeta;     // λ
     float beta_lbeta;// β·λ
+    float beta_4;    // β/4
+    float lbeta_4;   // λ/4
 };
 
 // MUFU exp2: ex2.approx.ftz.f32 (results below the normal range flush to +0).
@@ -76,6 +84,15 @@ __device__ __forceinline__ float tanh_num_small(float z, float onepE) {
 
 constexpr float kSmallZ = 0.0625f;
 
+// 1 - 2^t for t <= 0 given e = ex2(t): the series -t·ln2·(1 + t·ln2/2) for t > -0.0144 (|t·ln2| < 0.01,
+// truncation below 1.7e-5 relative), else the difference 1 - e (error below 1.7e-5 relative there).
+__device__ __forceinline__ float one_minus_exp2(float t, float e) {
+    constexpr float kLn2 = 0.6931471805599453f;
+    constexpr float kLn2Sq2 = 0.2402265069591007f;  // ln(2)^2 / 2
+    const float series = -t * fmaf(t, kLn2Sq2, kLn2);
+    return (t > -0.0144f) ? series : (1.0f - e);
+}
+
 // ---------------- forward: a = G·L ----------------
 
 // β == 4 (E2 = E1²). 2 ex2 + 1 rcp.
@@ -105,69 +122,62 @@ __device__ __forceinline__ float fwd_gen(float u, float v, const Coef& c) {
     return with_sign(m, sign_of(u) ^ sign_of(v));
 }
 
-// ---------------- backward: a, dgate, dlinear ----------------
-// pg = p·g (dL/da of this element); a is returned unrounded for the dp sum.
+// ---------------- backward: a/16, dgate, dlinear ----------------
+// pg16 = 16·p·g (16 times dL/da of this element); a16 = a/16 is returned unrounded for the dp sum.
 
 struct Bwd {
-    float a;
-    float dgate;
-    float dlin;
+    float a16;    // a / 16
+    float dgate;  // p·g·L·G'
+    float dlin;   // p·g·G·L'
 };
 
 // β == 4. 2 ex2 + 1 rcp.
-__device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg, const Coef& c) {
-    float E = ex2(fabsf(u) * c.k_tu);           // e^{−|u|/2}
-    float e = ex2(fabsf(v) * c.k_tv);           // e^{−2|v|/λ}
-    float E2 = E * E;                           // e^{−|u|}
-    float pE = 1.0f + E, pE2 = 1.0f + E2, pe = 1.0f + e;
-    float P = pE * pE2;
-    float r = rcp(P * pe);
-    float q = r * pe;                           // 1/((1+E)(1+E2))
-    float w = r * P;                            // 1/(1+e)
-    bool neg = u < 0.0f;
-    float s = neg ? E2 : 1.0f;
-    float omE = 1.0f - E;
-    uint32_t su = sign_of(u), sv = sign_of(v);
-    float G = with_sign(4.0f * omE * s * q, su);
-    float t2 = omE * pE * E2;                   // (1 − E2)·E2
-    float br = fmaf(E * s, pE2, neg ? -t2 : t2);
-    float Gp = 4.0f * q * q * br;
-    float L = with_sign(c.lbeta * (1.0f - e) * w, sv);
-    float Lp = 4.0f * e * w * w;
+__device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& c) {
+    const float tg = fabsf(u) * c.k_tu, tl = fabsf(v) * c.k_tv;
+    const float E = ex2(tg);                    // e^{−|u|/2}
+    const float e = ex2(tl);                    // e^{−2|v|/λ}
+    const float E2 = E * E;                     // e^{−|u|}
+    const float pE = 1.0f + E, pE2 = 1.0f + E2, pe = 1.0f + e;
+    const float P = pE * pE2;
+    const float r = rcp(P * pe);
+    const float q = r * pe;                     // 1/((1+E)(1+E2))
+    const float w = r * P;                      // 1/(1+e)
+    const float s = (u < 0.0f) ? E2 : 1.0f;
+    const float omE = one_minus_exp2(tg, E);    // 1 − E
+    const uint32_t su = sign_of(u), sv = sign_of(v);
+    const float G4 = with_sign(omE * s * q, su);                        // G/4
+    const float br = fmaf(E * s, pE2, with_sign(omE * pE * E2, su));    // G' = 4·q²·br
+    const float L4 = with_sign(c.lbeta_4 * one_minus_exp2(tl, e) * w, sv);  // L/4
     Bwd o;
-    o.a = G * L;
-    o.dgate = pg * L * Gp;
-    o.dlin = pg * G * Lp;
+    o.a16 = G4 * L4;
+    o.dgate = (pg16 * L4) * (q * q * br);
+    o.dlin = (pg16 * G4) * (e * (w * w));       // L' = 4·e·w²
     return o;
 }
 
 // Any β, λ. 3 ex2 + 1 rcp, small-argument series for both tanh numerators.
-__device__ __forceinline__ Bwd bwd_gen(float u, float v, float pg, const Coef& c) {
-    float au = fabsf(u), av = fabsf(v);
-    float E1 = ex2(au * c.k_tu);
-    float E2 = ex2(au * c.k_su);
-    float e = ex2(av * c.k_tv);
-    float pE1 = 1.0f + E1, pE2 = 1.0f + E2, pe = 1.0f + e;
-    float zu = au * c.inv_beta, zv = av * c.inv_lbeta;
-    float tn = (zu < kSmallZ) ? tanh_num_small(zu, pE1) : (1.0f - E1);
-    float wn = (zv < kSmallZ) ? tanh_num_small(zv, pe) : (1.0f - e);
-    float P = pE1 * pE2;
-    float r = rcp(P * pe);
-    float q = r * pe;
-    float w = r * P;
-    bool neg = u < 0.0f;
-    float s = neg ? E2 : 1.0f;
-    uint32_t su = sign_of(u), sv = sign_of(v);
-    float G = with_sign(c.beta * tn * s * q, su);
-    float t2 = c.beta * tn * pE1 * E2;          // β·(1 − E1²)·E2
-    float br = fmaf(4.0f * E1 * s, pE2, neg ? -t2 : t2);
-    float Gp = q * q * br;
-    float L = with_sign(c.lbeta * wn * w, sv);
-    float Lp = 4.0f * e * w * w;
+__device__ __forceinline__ Bwd bwd_gen(float u, float v, float pg16, const Coef& c) {
+    const float au = fabsf(u), av = fabsf(v);
+    const float E1 = ex2(au * c.k_tu);
+    const float E2 = ex2(au * c.k_su);
+    const float e = ex2(av * c.k_tv);
+    const float pE1 = 1.0f + E1, pE2 = 1.0f + E2, pe = 1.0f + e;
+    const float zu = au * c.inv_beta, zv = av * c.inv_lbeta;
+    const float tn = (zu < kSmallZ) ? tanh_num_small(zu, pE1) : (1.0f - E1);
+    const float wn = (zv < kSmallZ) ? tanh_num_small(zv, pe) : (1.0f - e);
+    const float P = pE1 * pE2;
+    const float r = rcp(P * pe);
+    const float q = r * pe;
+    const float w = r * P;
+    const float s = (u < 0.0f) ? E2 : 1.0f;
+    const uint32_t su = sign_of(u), sv = sign_of(v);
+    const float G4 = with_sign(c.beta_4 * tn * s * q, su);                          // G/4
+    const float br = fmaf(E1 * s, pE2, with_sign(c.beta_4 * tn * pE1 * E2, su));    // G' = 4·q²·br
+    const float L4 = with_sign(c.lbeta_4 * wn * w, sv);                             // L/4
     Bwd o;
-    o.a = G * L;
-    o.dgate = pg * L * Gp;
-    o.dlin = pg * G * Lp;
+    o.a16 = G4 * L4;
+    o.dgate = (pg16 * L4) * (q * q * br);
+    o.dlin = (pg16 * G4) * (e * (w * w));
     return o;
 }
 
@@ -177,8 +187,8 @@ __device__ __forceinline__ float fwd(float u, float v, const Coef& c) {
 }
 
 template <bool BETA4>
-__device__ __forceinline__ Bwd bwd(float u, float v, float pg, const Coef& c) {
-    return BETA4 ? bwd_b4(u, v, pg, c) : bwd_gen(u, v, pg, c);
+__device__ __forceinline__ Bwd bwd(float u, float v, float pg16, const Coef& c) {
+    return BETA4 ? bwd_b4(u, v, pg16, c) : bwd_gen(u, v, pg16, c);
 }
 
 }  // namespace situ

@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 0
+#define SITU_GLU_VERSION_MINOR 1
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -112,6 +112,53 @@ int situ_glu_fwd(const void* x, void* out, int64_t R, int64_t H, float beta, flo
  */
 int situ_glu_bwd_router(const void* x, const void* g, const float* p, void* dx, float* dp,
                         int64_t R, int64_t H, float beta, float lbeta, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Block-wise FP8 saved x.
+ *
+ * "Kimi K3 模型结构（9）：显存", section "统一激活管理器：重算、量化、offload 都是存储策略": most
+ * activations saved for the backward are stored with block-wise FP8 quantisation, while
+ * elementwise operators are recomputed. Here the saved tensor x is stored as OCP FP8 E4M3
+ * codes with one fp32 scale per block of SITU_GLU_FP8_BLOCK consecutive elements of one half
+ * of a row (the last block of a half may be shorter), which halves the saved bytes and cuts
+ * the backward's traffic from 10H + 8 to 8H + 8*ceil(H/128) + 8 bytes per row.
+ *
+ * For each block: a = max(amax(|x|), 448 * 2^-126), scale = a / 448,
+ * code = E4M3 round-to-nearest-even, saturated to +-448, of x * (448 / a); each step is one
+ * IEEE fp32 operation. Dequantised x^ = value(code) * scale (fp32).
+ *
+ * Layouts: xq uint8 [R, 2H] (gate codes then linear codes, like x); xs fp32 [R, 2*nb] with
+ * nb = ceil(H / SITU_GLU_FP8_BLOCK) (gate blocks, then linear blocks).
+ * A non-finite element makes its own code NaN; an infinity also makes its block's scale
+ * infinite (so the block dequantises to NaN).
+ * --------------------------------------------------------------------------------------- */
+#define SITU_GLU_FP8_BLOCK 128
+
+/*
+ * Forward that also saves x in FP8: out exactly as situ_glu_fwd, plus xq and xs from one read
+ * of x.
+ *   x      device, bf16 [R,2H], read only
+ *   out    device, bf16 [R,H], written
+ *   xq     device, uint8 [R,2H], written (8-byte alignment takes the vector path)
+ *   xs     device, fp32 [R,2*nb], written (4-byte aligned)
+ *   outputs must not overlap x or each other
+ *   R, H, beta, lbeta, stream as for situ_glu_fwd
+ */
+int situ_glu_fwd_save_fp8(const void* x, void* out, uint8_t* xq, float* xs, int64_t R, int64_t H,
+                          float beta, float lbeta, cudaStream_t stream);
+
+/*
+ * Fused backward + router gradient from the FP8-saved x: the formulas of situ_glu_bwd_router
+ * evaluated at x^ = value(xq) * xs.
+ *   xq, xs device, read only, as written by situ_glu_fwd_save_fp8
+ *   g, p   as for situ_glu_bwd_router
+ *   dx     device, bf16 [R,2H], written; dp device, fp32 [R], written; neither may overlap an
+ *          input or the other
+ *   R, H, beta, lbeta, stream as for situ_glu_fwd
+ */
+int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, const float* p,
+                            void* dx, float* dp, int64_t R, int64_t H, float beta, float lbeta,
+                            cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code (unknown codes included). */
 const char* situ_glu_status_string(int status);

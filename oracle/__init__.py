@@ -264,3 +264,34 @@ def dequantize_fp8(q, sc, block: int = FP8_BLOCK):
 def bwd_router_fp8(q, sc, g_bits, p, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0,
                    block: int = FP8_BLOCK):
     return _default().bwd_router_fp8(q, sc, g_bits, p, beta, lbeta, nthreads, block)
+
+
+# ---------------------------------------------------------------- fused down-projection dgrad
+
+def grouped_dgrad(dy_bits, wt_bits, offsets):
+    """g = dY·W_down per expert, in double: rows offsets[e]..offsets[e+1] of dY (bf16 bits
+    [R, D]) times W_down of expert e, given as its transpose wt_bits[e] = W_downᵀ (bf16 bits
+    [H, D]), so g[r, j] = Σ_d dY[r, d]·W_down,e[d, j] = Σ_d dY[r, d]·wt[e, j, d].
+
+    "Kimi K3 模型结构（9）：显存", section "MoE 反向…": (W_down,e)ᵀ·dL/dy is the quantity the
+    backward already computes on its way to a_e; here it is formed with numpy's fp64 matmul."""
+    dy = (np.ascontiguousarray(dy_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    wt = (np.ascontiguousarray(wt_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E, H, D = wt.shape
+    assert dy.shape[1] == D and offsets.shape == (E + 1,) and offsets[0] == 0 and offsets[-1] == dy.shape[0]
+    g = np.zeros((dy.shape[0], H), dtype=np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            g[a:b] = dy[a:b] @ wt[e].T
+    return g
+
+
+def dgrad_bwd_router(x_bits, dy_bits, wt_bits, offsets, p, beta: float = 4.0, lbeta: float = 25.0,
+                     nthreads: int = 0):
+    """Fused down-projection dgrad + SiTU-GLU backward + router gradient, in double:
+    g = grouped_dgrad(dY, W_downᵀ), then the backward of bwd_router_f64 at g (never rounded)."""
+    g = grouped_dgrad(dy_bits, wt_bits, offsets)
+    x = (np.ascontiguousarray(x_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return _default().bwd_router_f64(x, g, np.asarray(p, dtype=np.float32).astype(np.float64), beta, lbeta, nthreads)

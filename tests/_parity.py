@@ -3,9 +3,11 @@
 Acceptance (the stated tolerance of the method's port):
 * bf16 outputs (out, dx):  |gpu - ref| <= max(ulp_bf16(ref), 1e-3),
   ulp_bf16(ref) = 2^(floor(log2|ref|) - 7)  (0 for ref == 0, leaving the 1e-3 floor);
-* fp32 dp:  |gpu - ref| <= 1e-3·|ref| + 1e-6·Σ_j|g_j·a_j|.
+* fp32 dp:  |gpu - ref| <= 1e-3·|ref| + 1e-6·Σ_j|g_j·a_j| + 2^-126.
   The second term only matters where the row sum cancels to nearly zero, where a
   purely relative bound is ill-posed; the count of rows that needed it is reported.
+  The last is the smallest normal fp32: an fp32 result cannot resolve values below it.
+A NaN on one side must be a NaN on the other (non-finite inputs propagate).
 """
 from __future__ import annotations
 
@@ -19,6 +21,7 @@ import oracle
 BF16_ABS_FLOOR = 1e-3
 DP_REL = 1e-3
 DP_ABS_SCALE = 1e-6
+FP32_MIN_NORMAL = 2.0 ** -126
 
 
 def bits_of(t: torch.Tensor) -> np.ndarray:
@@ -80,18 +83,21 @@ class Parity:
 
     def dp(self, gpu: np.ndarray, ref: np.ndarray, ref_abs: np.ndarray, row0: int = 0):
         gpu = gpu.astype(np.float64)
-        err = np.abs(gpu - ref)
-        rel_tol = DP_REL * np.abs(ref)
-        tol = rel_tol + DP_ABS_SCALE * ref_abs
+        both_nan = np.isnan(gpu) & np.isnan(ref)
+        with np.errstate(invalid="ignore"):
+            err = np.where(both_nan, 0.0, np.abs(gpu - ref))
+            rel_tol = DP_REL * np.abs(ref)
+            tol = np.where(both_nan, 0.0, rel_tol + DP_ABS_SCALE * ref_abs + FP32_MIN_NORMAL)
         bad = ~(err <= tol)
         tl = self.t["dp"]
         tl.n += ref.size
         tl.bad += int(bad.sum())
-        tl.floor_rows += int(((err > rel_tol) & ~bad).sum())
+        with np.errstate(invalid="ignore"):
+            tl.floor_rows += int(((err > rel_tol) & ~bad).sum())
         if ref.size:
-            tl.worst_ratio = max(tl.worst_ratio, float(np.max(np.where(tol > 0, err / np.maximum(tol, 1e-300), 0))))
-            tl.worst_abs = max(tl.worst_abs, float(err.max()))
-            nz = np.abs(ref) > 0
+            tl.worst_ratio = max(tl.worst_ratio, float(np.nanmax(np.where(tol > 0, err / np.maximum(tol, 1e-300), 0))))
+            tl.worst_abs = max(tl.worst_abs, float(np.nanmax(err)))
+            nz = (np.abs(ref) > 0) & ~both_nan
             if nz.any():
                 tl.worst_rel = max(tl.worst_rel, float((err[nz] / np.abs(ref[nz])).max()))
         for i in np.nonzero(bad)[0][:5 - len(tl.examples)]:

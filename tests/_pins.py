@@ -412,3 +412,33 @@ def pin_fp8_backward_is_backward_of_dequantized(o):
     xh = o.dequantize_fp8(q, sc).astype(np.float64)
     dx2, dp2, _ = o.bwd_router_f64(xh, _bits_to_f32(gb).astype(np.float64), p.astype(np.float64))
     assert np.array_equal(dx, dx2) and np.array_equal(dp, dp2)
+
+
+# ---------------------------------------------------------------- fused down-projection dgrad
+
+def pin_grouped_dgrad(o_mod):
+    """The oracle's grouped dgrad equals a brute-force triple loop, experts with 0 rows included;
+    and the fused dp equals the naive router gradient <dL/dy, o_e> with stored o_e = W_e·a_e."""
+    rng = np.random.default_rng(12)
+    E, H, D = 4, 3, 5
+    counts = [2, 0, 3, 1]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    R = int(off[-1])
+    dy = _bf16_bits(rng.normal(0, 1, (R, D)))
+    wt = _bf16_bits(rng.normal(0, 0.5, (E, H, D)).reshape(E * H, D)).reshape(E, H, D)
+    x = _bf16_bits(rng.normal(0, 3, (R, 2 * H)))
+    p = rng.uniform(0.1, 1, R).astype(np.float32)
+    g = o_mod.grouped_dgrad(dy, wt, off)
+    dyf, wtf = _bits_to_f32(dy).astype(np.float64), _bits_to_f32(wt).astype(np.float64)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            for j in range(H):
+                ref = sum(dyf[r, d] * wtf[e, j, d] for d in range(D))
+                assert abs(g[r, j] - ref) <= 1e-12 * max(1.0, abs(ref))
+    dx, dp, _ = o_mod.dgrad_bwd_router(x, dy, wt, off, p)
+    a = o_mod.fwd_f64(_bits_to_f32(x).astype(np.float64))
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            o_e = wtf[e].T @ a[r]                          # o_e = W_down,e · a_e  (W_down,e = wt[e]ᵀ)
+            naive = float(dyf[r] @ o_e)                    # <dL/dy, o_e>
+            assert abs(dp[r] - naive) <= 1e-12 * max(1.0, abs(naive))

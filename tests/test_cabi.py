@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10000
+    assert sg.version() == 10100
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
@@ -131,3 +131,34 @@ def test_binding_fails_loudly_without_library(tmp_path, monkeypatch):
     monkeypatch.setattr(mod, "LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         mod.load()
+
+
+def fwd8(lib, x, out, xq, xs, R, H, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_fwd_save_fp8(x, out, xq, xs, R, H, beta, lbeta, None)
+
+
+def bwd8(lib, xq, xs, g, p, dx, dp, R, H, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_bwd_router_fp8(xq, xs, g, p, dx, dp, R, H, beta, lbeta, None)
+
+
+def test_fp8_entry_points_validate_before_any_launch(lib):
+    R, H = 4, 256                    # x 4096 B, out 2048 B, xq 2048 B, xs 4*2*2*4 = 64 B
+    x, out, xq, xs = A, A + (1 << 16), A + (2 << 16), A + (3 << 16)
+    assert fwd8(lib, None, None, None, None, 0, H) == OK
+    assert fwd8(lib, x, out, xq, xs, -1, H) == INVALID
+    assert fwd8(lib, x, out, xq, xs, R, 0) == INVALID
+    assert fwd8(lib, x, out, xq, xs, R, H, 0.0) == INVALID
+    assert fwd8(lib, x, out, None, xs, R, H) == INVALID
+    assert fwd8(lib, x, out, xq, xs + 2, R, H) == INVALID      # scales need 4-byte alignment
+    assert fwd8(lib, x + 1, out, xq, xs, R, H) == INVALID
+    assert fwd8(lib, x, out, x + 100, xs, R, H) == OVERLAP     # codes over x
+    assert fwd8(lib, x, out, xq, out + 64, R, H) == OVERLAP    # scales over out
+    assert fwd8(lib, x, out, out + 1024, xs, R, H) == OVERLAP  # codes over out
+    g, p, dx, dp = B, B + (1 << 16), B + (2 << 16), B + (3 << 16)
+    assert bwd8(lib, None, None, None, None, None, None, 0, H) == OK
+    assert bwd8(lib, xq, xs, g, p, dx, dp, R, -3) == INVALID
+    assert bwd8(lib, xq, None, g, p, dx, dp, R, H) == INVALID
+    assert bwd8(lib, xq, xs, g, p + 2, dx, dp, R, H) == INVALID
+    assert bwd8(lib, xq, xs, g, p, xq, dp, R, H) == OVERLAP      # dx over the codes
+    assert bwd8(lib, xq, xs, g, p, dx, xs, R, H) == OVERLAP      # dp over the scales
+    assert bwd8(lib, xq, xs, g, p, dx, dx + 8, R, H) == OVERLAP  # dp inside dx

@@ -88,3 +88,7 @@ def test_fp8_block_quantization():
 
 def test_fp8_backward_is_backward_of_dequantized():
     _pins.pin_fp8_backward_is_backward_of_dequantized(oracle)
+
+
+def test_grouped_dgrad():
+    _pins.pin_grouped_dgrad(oracle)

@@ -325,3 +325,158 @@ def test_binding_rejects_bad_tensors(sg):
         sg.situ_glu_bwd_router(xo, torch.zeros(4, 8, dtype=torch.bfloat16, device=DEV),
                                torch.zeros(4, device=DEV), dx=dxo)
     assert ei.value.status == 2
+
+
+# ---------------------------------------------------------------- block-wise FP8 saved x
+
+import oracle  # noqa: E402
+from _parity import compare_rows  # noqa: E402
+
+
+def run_fp8(sg, x, g, p, beta=4.0, lbeta=25.0):
+    out, xq, xs = sg.situ_glu_fwd_save_fp8(x, beta=beta, lbeta=lbeta)
+    dx, dp = sg.situ_glu_bwd_router_fp8(xq, xs, g, p, beta=beta, lbeta=lbeta)
+    torch.cuda.synchronize()
+    return out, xq, xs, dx, dp
+
+
+def check_fp8_rows(par, x, g, p, out, xq, xs, dx, dp, beta=4.0, lbeta=25.0, row0=0):
+    """Codes and scales bit-exact against the oracle's quantiser; out against the oracle's
+    forward; dx and dp against the oracle's backward at the dequantised x."""
+    xb = bits_of(x)
+    q_ref, s_ref = oracle.quantize_fp8(xb)
+    q_gpu = xq.detach().cpu().numpy()
+    s_gpu = xs.detach().cpu().numpy()
+    nq = int((q_gpu != q_ref).sum())
+    ns = int((s_gpu.view(np.uint32) != s_ref.view(np.uint32)).sum())
+    assert nq == 0, f"{par.name}: {nq} FP8 codes differ from the oracle, rows from {row0}"
+    assert ns == 0, f"{par.name}: {ns} FP8 scales differ from the oracle, rows from {row0}"
+    par.bf16("out", bits_of(out), oracle.fwd_bf16(xb, beta, lbeta), row0)
+    dx_ref, dp_ref, dpa = oracle.bwd_router_fp8(q_ref, s_ref, bits_of(g), p.detach().cpu().numpy(), beta, lbeta)
+    par.bf16("dx", bits_of(dx), dx_ref, row0)
+    par.dp(dp.detach().cpu().numpy(), dp_ref, dpa, row0)
+
+
+def check_fp8_full(par, x, g, p, out, xq, xs, dx, dp, beta=4.0, lbeta=25.0, chunk_rows=8192):
+    for a in range(0, x.shape[0], chunk_rows):
+        b = min(x.shape[0], a + chunk_rows)
+        check_fp8_rows(par, x[a:b], g[a:b], p[a:b], out[a:b], xq[a:b], xs[a:b], dx[a:b], dp[a:b], beta, lbeta, a)
+
+
+@pytest.mark.parametrize("name", ["routed_r1024_h3072", "saturating_mix_r16384_h3072"])
+def test_fp8_workload_all_rows(sg, name):
+    w = si.get(name)
+    x, g, p = on_device(w)
+    out, xq, xs, dx, dp = run_fp8(sg, x, g, p)
+    par = Parity("fp8 " + name)
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+    # the forward output is exactly the bf16-saved forward's
+    assert torch.equal(out.view(torch.int16), sg.situ_glu_fwd(x).view(torch.int16))
+
+
+@pytest.mark.parametrize("H", si.TAIL_SWEEP_H)
+@pytest.mark.parametrize("R", [1, 37, 65537])
+def test_fp8_tail_sweep_all_rows(sg, R, H):
+    w = si.tail_sweep(R, H)
+    x, g, p = on_device(w)
+    out, xq, xs, dx, dp = run_fp8(sg, x, g, p)
+    par = Parity("fp8 " + w.name)
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+
+
+@pytest.mark.slow
+def test_fp8_pages_scale_full_launch_sampled_rows(sg):
+    w = si.get("pages_scale_r1600000_h3072")
+    x, g, p = on_device(w, gen_on_device=True)
+    out, xq, xs, dx, dp = run_fp8(sg, x, g, p)
+    del out
+    assert bool(torch.isfinite(dx).all()) and bool(torch.isfinite(dp).all()) and bool(torch.isfinite(xs).all())
+    rows = sample_rows(w.R, n_random=2048, seed=5).to(x.device)
+    take = lambda t: t.index_select(0, rows)
+    out_s = sg.situ_glu_fwd(take(x))
+    par = Parity(w.name + " fp8 (sampled)")
+    check_fp8_rows(par, take(x), take(g), take(p), out_s, take(xq), take(xs), take(dx), take(dp))
+    par.assert_ok()
+    free(x, g, p, xq, xs, dx, dp)
+
+
+@pytest.mark.parametrize("beta,lbeta", [(4.0, 25.0), (2.5, 7.0)])
+@pytest.mark.parametrize("H", [1, 7, 8, 16, 128, 130, 136, 999])
+def test_fp8_odd_widths(sg, H, beta, lbeta):
+    w = si.custom(37, H, seed=100 + H, x_std=4.0)
+    x, g, p = on_device(w)
+    out, xq, xs, dx, dp = run_fp8(sg, x, g, p, beta, lbeta)
+    par = Parity(f"fp8 H={H} beta={beta}")
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp, beta, lbeta)
+    par.assert_ok()
+
+
+def test_fp8_zero_tiny_and_huge_blocks(sg):
+    H = 384
+    x = torch.zeros(5, 2 * H, dtype=torch.float32)
+    x[1] = torch.linspace(-1e-37, 1e-37, 2 * H)          # below the amax floor: scale 2^-126
+    x[2] = torch.linspace(-1.0, 1.0, 2 * H) * 3e38       # near the bf16 maximum
+    x[3, ::7] = 5.0                                       # sparse block contents
+    x[4] = torch.randn(2 * H, generator=torch.Generator().manual_seed(1)) * 1e-3
+    x = x.to(torch.bfloat16).to(DEV)
+    g = torch.ones(5, H, dtype=torch.bfloat16, device=DEV)
+    p = torch.full((5,), 0.25, device=DEV)
+    out, xq, xs, dx, dp = run_fp8(sg, x, g, p)
+    assert float(xs[0].min()) == float(xs[0].max()) == 2.0 ** -126 and int(xq[0].max()) == 0
+    par = Parity("fp8 zero/tiny/huge")
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+
+
+def test_fp8_misaligned_codes_take_the_element_path(sg):
+    R, H = 9, 1000
+    w = si.custom(R, H, seed=3)
+    x, g, p = on_device(w)
+    qb = torch.empty(R * 2 * H + 16, dtype=torch.uint8, device=DEV)
+    xq = qb[1:1 + R * 2 * H].view(R, 2 * H)              # 1 byte past an 8-byte boundary
+    out, xq, xs = sg.situ_glu_fwd_save_fp8(x, xq=xq)
+    dx, dp = sg.situ_glu_bwd_router_fp8(xq, xs, g, p)
+    torch.cuda.synchronize()
+    par = Parity("fp8 misaligned codes")
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+    ref = run_fp8(sg, x, g, p)                            # aligned vector path: same codes and dx
+    assert torch.equal(ref[1], xq) and torch.equal(ref[2], xs)
+    assert torch.equal(ref[3].view(torch.int16), dx.view(torch.int16))
+
+
+def test_fp8_guard_bands_untouched(sg):
+    R, H, pad = 37, 1000, 64
+    nb = sg.fp8_scale_blocks(H)
+    w = si.custom(R, H, seed=6)
+    x, g, p = on_device(w)
+    qb = torch.full((R * 2 * H + 2 * pad,), 0xA5, dtype=torch.uint8, device=DEV)
+    sb = torch.full((R * 2 * nb + 2 * pad,), float("nan"), dtype=torch.float32, device=DEV)
+    xq = qb[pad:pad + R * 2 * H].view(R, 2 * H)
+    xs = sb[pad:pad + R * 2 * nb].view(R, 2 * nb)
+    out, _, _ = sg.situ_glu_fwd_save_fp8(x, xq=xq, xs=xs)
+    dx, dp = sg.situ_glu_bwd_router_fp8(xq, xs, g, p)
+    torch.cuda.synchronize()
+    assert bool((qb[:pad] == 0xA5).all()) and bool((qb[pad + R * 2 * H:] == 0xA5).all())
+    assert bool(torch.isnan(sb[:pad]).all()) and bool(torch.isnan(sb[pad + R * 2 * nb:]).all())
+    par = Parity("fp8 guarded")
+    check_fp8_full(par, x, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+
+
+@pytest.mark.parametrize("scale", [1e-3, 3e-2, 1e-5])
+def test_small_magnitude_rows(sg, scale):
+    """Rows of small pre-activations: the backward's dp keeps its relative tolerance (the
+    numerators 1 - e^{-y} are evaluated by a series for small y instead of as a difference)."""
+    w = si.custom(512, 3072, seed=int(1 / scale) % 997, x_std=scale)
+    x, g, p = on_device(w)
+    out, dx, dp = run(sg, x, g, p)
+    par = Parity(f"small magnitude x ~ N(0, {scale}^2)")
+    compare_full(par, x, g, p, out, dx, dp)
+    par.assert_ok()
+    out8, xq, xs, dx8, dp8 = run_fp8(sg, x, g, p)
+    par8 = Parity(f"fp8, small magnitude x ~ N(0, {scale}^2)")
+    check_fp8_full(par8, x, g, p, out8, xq, xs, dx8, dp8)
+    par8.assert_ok()
