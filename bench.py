@@ -64,6 +64,10 @@ def parse_args(argv=None):
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 saved-x variant's timing")
+    ap.add_argument("--no-dgrad", action="store_true", help="skip the fused dgrad GEMM's timing")
+    ap.add_argument("--only-dgrad", action="store_true", help="time only the fused dgrad GEMM (profiling runs)")
+    ap.add_argument("--dgrad-rows", type=int, default=None, help="rows split evenly over --dgrad-experts")
+    ap.add_argument("--dgrad-experts", type=int, default=None)
     ap.add_argument("--rows", type=int, default=None, help="override R (for small profiling runs)")
     return ap.parse_args(argv)
 
@@ -260,6 +264,20 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- native arm
 
+def run_dgrad_only(args):
+    import torch
+
+    import bwd_situ_glu_gb300 as sg
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    sg.build()
+    sg.load()
+    peak, _ = load_peaks()
+    res = time_dgrad(sg, dev, args.steps, args.warmup, peak, rows=args.dgrad_rows, experts=args.dgrad_experts)
+    print(json.dumps({"dgrad_fused": res}), flush=True)
+    return 0 if res["status"] == 0 else 1
+
+
 def run_native(args):
     import torch
 
@@ -340,6 +358,7 @@ def run_native(args):
     step_gbs = (fwd_bytes + bwd_bytes) / (elapsed_ms / K * 1e-3) / 1e9
 
     fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
+    dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak)
 
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_hash() and NCU_TRAFFIC["bwd_bytes_per_row"]:
@@ -393,6 +412,7 @@ def run_native(args):
         "e2e": e2e,
         "cpu_baseline": cpu,
         "fp8_saved_x": fp8,
+        "dgrad_fused": dgrad,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -441,6 +461,74 @@ def time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, warmup, peak):
             "rows_per_s": R / ((f_ms + b_ms) * 1e-3),
             "saved_bytes_per_row": {"bf16_x": 4 * H, "fp8_x": 2 * H + 8 * nb},
             "gpu_launches": 2 * steps}
+
+
+def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, experts=None):
+    """Fused down-projection dgrad (tcgen05 grouped GEMM) + backward + router gradient on the
+    expert-grouped workload: 16384 tokens x top-16 of 896 experts, rows grouped by expert,
+    H = 3072, D = 3584 (the expert output width), synthetic N(0, 1/D) weights.
+    With rows and experts given: that many rows split evenly over that many experts instead."""
+    import numpy as np
+    import torch
+
+    import situ_inputs as si
+    w = si.get("expert_grouped_r262144_h3072")
+    if rows and experts:
+        E = experts
+        counts = np.full(E, rows // E, dtype=np.int64)
+        counts[: rows % E] += 1
+        p = torch.rand(rows, generator=torch.Generator().manual_seed(seed))
+        R, H = rows, w.H
+        workload = f"uniform_r{rows}_e{E}_h{H}_d{D}"
+    else:
+        p, experts_of_row, _ = si.router_rows(w.tokens, w.seed, order="expert")
+        counts = np.bincount(experts_of_row.numpy(), minlength=si.N_EXPERTS)
+        R, H, E = w.R, w.H, si.N_EXPERTS
+        workload = f"expert_grouped_r{R}_h{H} x D={D}, {E} experts"
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    x = (torch.randn(R, 2 * H, generator=gen, device=dev) * w.x_std).to(torch.bfloat16)
+    dy = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
+    for a in range(0, R, 32768):
+        dy[a:a + 32768] = torch.randn(min(32768, R - a), D, generator=gen, device=dev).to(torch.bfloat16)
+    wt = torch.empty(E, H, D, dtype=torch.bfloat16, device=dev)
+    for e in range(E):
+        wt[e] = (torch.randn(H, D, generator=gen, device=dev) / D ** 0.5).to(torch.bfloat16)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=dev)
+    p = p.to(dev)
+    dx = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
+    dp = torch.empty(R, dtype=torch.float32, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(max(1, warmup)):
+        sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx, dp, status=status)
+    torch.cuda.synchronize(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx, dp, status=status)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = e0.elapsed_time(e1) / steps
+    flops = 2.0 * R * D * H
+    nbytes = R * D * 2 + E * H * D * 2 + R * 4 * H + R * 4 * H + R * 8 + (E + 1) * 8
+    tf_peak = None
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            tf_peak = float(json.load(f)["bf16_tflops"])
+    except (OSError, KeyError, ValueError):
+        tf_peak = 1900.0
+    t_flop = flops / (tf_peak * 1e12) * 1e3
+    t_byte = nbytes / (hbm_peak * 1e9) * 1e3
+    bound = "tensor" if t_flop >= t_byte else "hbm"
+    del x, dy, wt, dx, dp
+    torch.cuda.empty_cache()
+    return {"workload": workload,
+            "ms": ms, "TFLOP_s": flops / ms / 1e9, "frac_of_bf16_peak": flops / ms / 1e9 / tf_peak,
+            "GB_s": nbytes / ms / 1e6, "frac_of_hbm_peak": nbytes / ms / 1e6 / hbm_peak,
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "bound": bound,
+            "roofline_frac": max(t_flop, t_byte) / ms, "status": int(status.item()),
+            "gpu_launches": steps}
 
 
 def pinned_like(t):
@@ -544,6 +632,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.only_dgrad:
+        return run_dgrad_only(args)
     return run_native(args)
 
 

@@ -28,7 +28,8 @@ CSRC = os.path.join(_HERE, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
-SOURCES = [os.path.join(CSRC, "situ_glu.cu"), os.path.join(CSRC, "situ_glu_fp8.cu")]
+SOURCES = [os.path.join(CSRC, "situ_glu.cu"), os.path.join(CSRC, "situ_glu_fp8.cu"),
+           os.path.join(CSRC, "situ_glu_dgrad.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h")] + [
     os.path.join(INCLUDE, "situ_glu.h")]
 
@@ -88,6 +89,8 @@ def load():
     lib.situ_glu_fwd_save_fp8.restype = cint
     lib.situ_glu_bwd_router_fp8.argtypes = [vp, vp, vp, vp, vp, vp, i64, i64, f32, f32, vp]
     lib.situ_glu_bwd_router_fp8.restype = cint
+    lib.situ_glu_bwd_router_dgrad.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp]
+    lib.situ_glu_bwd_router_dgrad.restype = cint
     lib.situ_glu_status_string.argtypes = [cint]
     lib.situ_glu_status_string.restype = ctypes.c_char_p
     lib.situ_glu_last_cuda_error.argtypes = []
@@ -246,9 +249,45 @@ def situ_glu_bwd_router_fp8(xq, xs, g, p, dx=None, dp=None, beta: float = 4.0, l
     return dx, dp
 
 
+def situ_glu_bwd_router_dgrad(x, dy, w_down_t, expert_offsets, p, dx=None, dp=None, status=None, beta: float = 4.0,
+                              lbeta: float = 25.0, stream=None):
+    """(dx bf16 [R,2H], dp fp32 [R]) from dY [R,D] and the experts' W_downᵀ [E,H,D]: the dgrad GEMM
+    g = dY·W_down,e on the tensor cores with the backward + router gradient fused into it.
+    ``status`` (int32 [1] on the device, zeroed by the caller) turns 1 if a pipeline wait timed out."""
+    import torch
+    if x.dim() != 2 or x.shape[1] % 2 != 0:
+        raise ValueError("x must be [R, 2H]")
+    R, H = x.shape[0], x.shape[1] // 2
+    if w_down_t.dim() != 3:
+        raise ValueError("w_down_t must be [E, H, D]")
+    E, D = w_down_t.shape[0], w_down_t.shape[2]
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    _need(dy, torch.bfloat16, (R, D), "dy")
+    _need(w_down_t, torch.bfloat16, (E, H, D), "w_down_t")
+    _need(expert_offsets, torch.int64, (E + 1,), "expert_offsets")
+    _need(p, torch.float32, (R,), "p")
+    if dx is None:
+        dx = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=x.device)
+    if dp is None:
+        dp = torch.empty((R,), dtype=torch.float32, device=x.device)
+    _need(dx, torch.bfloat16, (R, 2 * H), "dx")
+    _need(dp, torch.float32, (R,), "dp")
+    sptr = 0
+    if status is not None:
+        _need(status, torch.int32, (1,), "status")
+        sptr = status.data_ptr()
+    with torch.cuda.device(x.device):
+        _check(load().situ_glu_bwd_router_dgrad(x.data_ptr(), dy.data_ptr(), w_down_t.data_ptr(),
+                                                expert_offsets.data_ptr(), E, p.data_ptr(), dx.data_ptr(),
+                                                dp.data_ptr(), sptr, R, H, D, beta, lbeta,
+                                                _stream_handle(stream, x.device)))
+    return dx, dp
+
+
 __all__ = [
     "build", "load", "version", "status_string", "SituGluError",
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
+    "situ_glu_bwd_router_dgrad",
     "LIB_PATH", "INCLUDE",
 ]

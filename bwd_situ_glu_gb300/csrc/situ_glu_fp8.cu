@@ -255,6 +255,82 @@ __global__ void __launch_bounds__(TPB, 1) bwd_fp8_vec_kernel(const Codes8* __res
     }
 }
 
+// 16 codes (one 16-element chunk) as four 32-bit words.
+struct Codes16 {
+    uint32_t w[4];
+};
+
+__device__ __forceinline__ Codes16 ld_codes16(const Codes16* p) {
+    Codes16 v;
+    asm("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];"
+        : "=r"(v.w[0]), "=r"(v.w[1]), "=r"(v.w[2]), "=r"(v.w[3])
+        : "l"(p));
+    return v;
+}
+
+// Wide path: H % 16 == 0; xq 16-byte, g and dx 32-byte aligned. A lane takes 16 elements per
+// step (16 bytes of codes per half, 32 bytes of g); a warp step covers four scale blocks, one per
+// group of 8 lanes. For beta = 4 the dequantisation scale folds into the exponent arguments:
+// u enters the backward only through |u|·k_tu and its sign, so t = |value(code)|·(scale·k_tu)
+// replaces value·scale followed by |·|·k_tu (one fp32 rounding less than the oracle's two).
+template <bool BETA4, int TPB>
+__global__ void __launch_bounds__(TPB, 1) bwd_fp8_wide_kernel(const Codes16* __restrict__ xq,
+                                                              const float* __restrict__ xs,
+                                                              const Vec<8>* __restrict__ g,
+                                                              const float* __restrict__ p, Vec<8>* __restrict__ dx,
+                                                              float* __restrict__ dp, int64_t R, int cpr, int nb,
+                                                              Coef c) {
+    const int lane = threadIdx.x & 31;
+    const int64_t warp0 = ((int64_t)blockIdx.x * TPB + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * TPB) >> 5;
+    for (int64_t r = warp0; r < R; r += nwarps) {
+        const Codes16* qg = xq + r * (2 * (int64_t)cpr);
+        const Codes16* ql = qg + cpr;
+        const float* sg = xs + r * (2 * (int64_t)nb);
+        const float* sl = sg + nb;
+        const Vec<8>* gr = g + r * (int64_t)cpr;
+        Vec<8>* dgr = dx + r * (2 * (int64_t)cpr);
+        Vec<8>* dlr = dgr + cpr;
+        const float pr = 16.0f * p[r];   // 16·p: see situ::Bwd
+        float acc = 0.0f;
+        for (int c0 = 0; c0 < cpr; c0 += 32) {
+            const int ci = c0 + lane;
+            if (ci < cpr) {
+                const Codes16 qgv = ld_codes16(qg + ci), qlv = ld_codes16(ql + ci);
+                const Vec<8> yv = ld_stream<8, true, true>(gr + ci);
+                const float scg = sg[ci >> 3], scl = sl[ci >> 3];
+                const float kg = scg * c.k_tu, kl = scl * c.k_tv;
+                Vec<8> dgo, dlo;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint16_t cgi = (uint16_t)(qgv.w[i >> 1] >> (16 * (i & 1)));
+                    const uint16_t cli = (uint16_t)(qlv.w[i >> 1] >> (16 * (i & 1)));
+                    float u0, u1, v0, v1;
+                    e4m3x2_to_f32(cgi, u0, u1);
+                    e4m3x2_to_f32(cli, v0, v1);
+                    const float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
+                    situ::Bwd b0, b1;
+                    if constexpr (BETA4) {
+                        b0 = situ::bwd_b4_t(fabsf(u0) * kg, fabsf(v0) * kl, sign_of(u0), sign_of(v0), pr * g0, c);
+                        b1 = situ::bwd_b4_t(fabsf(u1) * kg, fabsf(v1) * kl, sign_of(u1), sign_of(v1), pr * g1, c);
+                    } else {
+                        b0 = situ::bwd_gen(__fmul_rn(u0, scg), __fmul_rn(v0, scl), pr * g0, c);
+                        b1 = situ::bwd_gen(__fmul_rn(u1, scg), __fmul_rn(v1, scl), pr * g1, c);
+                    }
+                    acc = fmaf(g0, b0.a16, acc);
+                    acc = fmaf(g1, b1.a16, acc);
+                    dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
+                    dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
+                }
+                st_stream<8>(dgr + ci, dgo);
+                st_stream<8>(dlr + ci, dlo);
+            }
+        }
+        acc = warp_sum(acc);
+        if (lane == 0) dp[r] = 16.0f * acc;
+    }
+}
+
 // Element path: any H.
 template <bool BETA4>
 __global__ void __launch_bounds__(kElemThreads) bwd_fp8_elem_kernel(const uint8_t* __restrict__ xq,
@@ -345,6 +421,17 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
+    if (H % 16 == 0 && aligned(xq, 16) && aligned(g, 32) && aligned(dx, 32)) {
+        const int cpr = (int)(H / 16);
+        const Codes16* qv = (const Codes16*)xq;
+        const Vec<8>* gv = (const Vec<8>*)g;
+        Vec<8>* dxv = (Vec<8>*)dx;
+        if (b4)
+            return launch(bwd_fp8_wide_kernel<true, kFp8Tpb>, kFp8Tpb, R, stream, qv, xs, gv, p, dxv, dp, R, cpr,
+                          (int)nb, c);
+        return launch(bwd_fp8_wide_kernel<false, kFp8Tpb>, kFp8Tpb, R, stream, qv, xs, gv, p, dxv, dp, R, cpr,
+                      (int)nb, c);
+    }
     if (H % 8 == 0 && aligned(xq, 8) && aligned(g, 16) && aligned(dx, 16)) {
         const int cpr = (int)(H / 8);
         const Codes8* qv = (const Codes8*)xq;

@@ -131,9 +131,9 @@ struct Bwd {
     float dlin;   // p·g·G·L'
 };
 
-// β == 4. 2 ex2 + 1 rcp.
-__device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& c) {
-    const float tg = fabsf(u) * c.k_tu, tl = fabsf(v) * c.k_tv;
+// β == 4 from the exponent arguments tg = |u|·k_tu, tl = |v|·k_tv and the sign bits of u and v
+// (the only ways u and v enter). 2 ex2 + 1 rcp.
+__device__ __forceinline__ Bwd bwd_b4_t(float tg, float tl, uint32_t su, uint32_t sv, float pg16, const Coef& c) {
     const float E = ex2(tg);                    // e^{−|u|/2}
     const float e = ex2(tl);                    // e^{−2|v|/λ}
     const float E2 = E * E;                     // e^{−|u|}
@@ -142,9 +142,8 @@ __device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& 
     const float r = rcp(P * pe);
     const float q = r * pe;                     // 1/((1+E)(1+E2))
     const float w = r * P;                      // 1/(1+e)
-    const float s = (u < 0.0f) ? E2 : 1.0f;
+    const float s = su ? E2 : 1.0f;             // σ numerator (u = −0 gives E2 = 1 as well)
     const float omE = one_minus_exp2(tg, E);    // 1 − E
-    const uint32_t su = sign_of(u), sv = sign_of(v);
     const float G4 = with_sign(omE * s * q, su);                        // G/4
     const float br = fmaf(E * s, pE2, with_sign(omE * pE * E2, su));    // G' = 4·q²·br
     const float L4 = with_sign(c.lbeta_4 * one_minus_exp2(tl, e) * w, sv);  // L/4
@@ -153,6 +152,11 @@ __device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& 
     o.dgate = (pg16 * L4) * (q * q * br);
     o.dlin = (pg16 * G4) * (e * (w * w));       // L' = 4·e·w²
     return o;
+}
+
+// β == 4. 2 ex2 + 1 rcp.
+__device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& c) {
+    return bwd_b4_t(fabsf(u) * c.k_tu, fabsf(v) * c.k_tv, sign_of(u), sign_of(v), pg16, c);
 }
 
 // Any β, λ. 3 ex2 + 1 rcp, small-argument series for both tanh numerators.

@@ -160,6 +160,35 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
                             void* dx, float* dp, int64_t R, int64_t H, float beta, float lbeta,
                             cudaStream_t stream);
 
+/* ---------------------------------------------------------------------------------------
+ * Down-projection dgrad fused with the backward (tensor cores).
+ *
+ * "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出": the routed row's
+ * g = (W_down,e)ᵀ·dL/dy is what the backward computes anyway; the router gradient and dL/da_e
+ * follow from it and a_e. This entry point computes g = dY·W_down,e for every expert's rows on
+ * the tensor cores (tcgen05, fp32 accumulation in tensor memory) and, in the same kernel, the
+ * outputs of situ_glu_bwd_router from that g (fp32, never rounded or written) and x.
+ *
+ *   x          device, bf16 [R,2H], read only (the saved forward input)
+ *   dy         device, bf16 [R,D], read only: dL/dy of each routed row (D = expert output width)
+ *   w_down_t   device, bf16 [E,H,D], read only: (W_down,e)ᵀ of each expert, K-major (row j of
+ *              expert e holds W_down,e[:, j]), so g[r,j] = Σ_d dy[r,d]·w_down_t[e,j,d]
+ *   expert_offsets device, int64 [E+1]: rows of expert e are expert_offsets[e] ..
+ *              expert_offsets[e+1]-1 (non-decreasing, from 0 to R; rows grouped by expert).
+ *              Malformed offsets give undefined results but no access outside the buffers.
+ *   p, dx, dp  as for situ_glu_bwd_router
+ *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
+ *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.
+ *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 4096, R < 2^31, E*H < 2^31
+ *   Pointers to x, dy, w_down_t, dx must be 16-byte aligned (TMA and vector access).
+ * Returns SITU_GLU_INVALID_ARG for shapes or alignments outside these limits (there is no
+ * general-shape fallback for this entry point).
+ * --------------------------------------------------------------------------------------- */
+int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_t,
+                              const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
+                              float* dp, int* status, int64_t R, int64_t H, int64_t D, float beta,
+                              float lbeta, cudaStream_t stream);
+
 /* Static, NUL-terminated description of a status code (unknown codes included). */
 const char* situ_glu_status_string(int status);
 
