@@ -38,9 +38,9 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum), per row, and the hash of the kernel source it was taken on.
 # Reported only while the source is unchanged; otherwise null.
 NCU_TRAFFIC = {
-    "source_sha256": "9f7c664e56b8cbb9fe2c8fd53fdf809a8de15e2f365bf7b3ddd9b290ef62cdca",
-    "bwd_bytes_per_row": (1.208400e9 + 0.7679488e9) / 65536,
-    "fwd_bytes_per_row": (0.805347e9 + 0.365363712e9) / 65536,
+    "source_sha256": "ec21a529bb2653914f7ae1ff9c89256ff96d1acbfcc0a7aaf928f02d1d13056b",
+    "bwd_bytes_per_row": (1.208449e9 + 0.769850368e9) / 65536,
+    "fwd_bytes_per_row": (0.805462e9 + 0.3650048e9) / 65536,
     "capture": "ncu --set full, R=65536 H=3072, scaled by rows (profiles/situ_glu_fwd_bwd_ncu_full_r65536_h3072.md)",
 }
 

@@ -15,9 +15,10 @@
 //   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one thread
 //               issues tcgen05.mma (M = 128, N = 256, K = 16), committing to mbarriers that free
 //               ring stages and hand finished accumulators to the epilogue;
-//   warps 2-9   epilogue: each warp owns one 32-lane TMEM quadrant and half of the 256 columns;
-//               a thread owns one row, reads its g with tcgen05.ld, loads the matching x, and
-//               writes dx; its dp partial stays in a register across the N-tiles of the row.
+//   warps 2..   epilogue, EPW warps per 32-lane TMEM quadrant, each with a slice of the 256 columns;
+//               a thread owns one row, reads its g with tcgen05.ld, loads the matching x (prefetched
+//               one chunk ahead), and writes dx; its dp partial stays in a register across the
+//               N-tiles of the row.
 // Every mbarrier wait is bounded: on a timeout the CTA records a non-zero status, stops issuing,
 // drains what it issued, frees TMEM and returns.
 #include <cuda.h>
@@ -43,8 +44,14 @@ constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int NUM_THREADS = 320;             // 10 warps
-constexpr int NUM_EPI_THREADS = 256;         // warps 2..9
+constexpr int EPW = 2;                       // epilogue warps per 32-lane TMEM quadrant
+constexpr int CW = 32;                       // accumulator columns per tcgen05.ld chunk
+constexpr int NUM_EPI_THREADS = 4 * EPW * 32;
+constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;  // warp 0 TMA, warp 1 MMA, then the epilogue
+constexpr int COLS_PER_WARP = BN / EPW;      // accumulator columns of one job an epilogue warp owns
+constexpr int CPJ = COLS_PER_WARP / CW;      // chunks per job per epilogue warp
+constexpr int XV = CW / 16;                  // 32-byte vectors (16 bf16) per half-row per chunk
+static_assert(CPJ >= 2 && CPJ % 2 == 0, "the x prefetch alternates two register buffers");
 constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 columns
 constexpr int MAX_EXPERTS = 4096;
 constexpr uint32_t WAIT_LIMIT = 1u << 22;    // polls of a try_wait before giving up (~1-2 s)
@@ -59,7 +66,7 @@ struct alignas(8) Barriers {
     uint32_t tmem_base;
     int abort;
 };
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Barriers) + 2 * BM * 4 +
+constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Barriers) + EPW * BM * 4 +
                            (MAX_EXPERTS + 1) * 4 + 64;
 
 // ---------------------------------------------------------------- PTX wrappers
@@ -142,20 +149,31 @@ __device__ __forceinline__ void tc_commit(uint64_t* bar) {
                  : "memory");
 }
 
-// 32 consecutive fp32 columns of this thread's TMEM lane.
-__device__ __forceinline__ void tc_ld32(uint32_t taddr, float (&v)[32]) {
-    uint32_t r[32];
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
-        "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
-          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
-        : "r"(taddr));
+// N consecutive fp32 columns (N = 16 or 32) of this thread's TMEM lane, waited for.
+template <int N>
+__device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[N]) {
+    uint32_t r[N];
+    if constexpr (N == 32) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+            "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr));
+    } else {
+        static_assert(N == 16, "16 or 32 columns");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    }
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 #pragma unroll
-    for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
 }
 
 __device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_THREADS) : "memory"); }
@@ -185,8 +203,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
     uint8_t* ring = smem;                                            // STAGES x (A | B)
     Barriers* bars = (Barriers*)(smem + STAGES * STAGE_BYTES);
-    float* dp_half = (float*)(bars + 1);                             // [BM] partials of the second column half
-    int* tile_start = (int*)(dp_half + 2 * BM);                      // [E + 1]
+    float* dp_part = (float*)(bars + 1);                             // [EPW][BM] per-warp-slot dp partials
+    int* tile_start = (int*)(dp_part + EPW * BM);                    // [E + 1]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = (int)(H / BN);
@@ -312,10 +330,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (mbar_try_wait(&bars->mma_done, 0)) break;
         }
     } else {
-        // ------------------------------------------------ epilogue (warps 2..9)
-        const int quad = warp & 3;                 // TMEM lane quadrant this warp may access
-        const int half = (warp - 2) >> 2;          // columns [0,128) or [128,256) of each job
+        // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
+        // A warp may read only the TMEM lanes of quadrant warp % 4; the EPW warps of a quadrant split
+        // each job's 256 columns into EPW slices of COLS_PER_WARP, read CW columns at a time. One
+        // thread owns one row for a whole M-tile: its x is fetched with 32-byte loads one chunk ahead
+        // (across job boundaries too, as x does not depend on the accumulator), so the loads are in
+        // flight while the previous chunk is computed and while the next accumulator is awaited.
+        const int quad = warp & 3;
+        const int slot = (warp - 2) >> 2;
         const int lrow = quad * 32 + lane;         // row within the tile
+        const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
         int job = 0;
         bool ok = true;
         for (int t = blockIdx.x; t < T; t += gridDim.x) {
@@ -325,54 +349,73 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = row0 + lrow;
             const bool valid = ok && row >= 0 && row < row_end;
             const float pr16 = valid ? 16.0f * p[row] : 0.0f;
-            const uint16_t* xr = x + (valid ? row : 0) * 2 * H;
-            uint16_t* dxr = dx + (valid ? row : 0) * 2 * H;
+            const uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * COLS_PER_WARP;
+            uint16_t* dxr = dx + (valid ? row : 0) * 2 * H + slot * COLS_PER_WARP;
             float acc_dp = 0.0f;
+            Vec<8> xb[2][2][XV];                   // [buffer][gate, linear][32-byte vector]
+            if (valid) {
+#pragma unroll
+                for (int v = 0; v < XV; ++v) {
+                    xb[0][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + 16 * v));
+                    xb[0][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + 16 * v));
+                }
+            }
             for (int nt = 0; nt < NT; ++nt, ++job) {
                 const int acc = job & 1;
                 const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
                 if (ok && !mbar_wait(&bars->tfull[acc], acc_phase, bars, status)) ok = false;
                 ok = __all_sync(0xffffffffu, ok);                 // tcgen05.ld below is warp-collective
                 tc_fence_after();
-                if (ok) {
-#pragma unroll 1
-                    for (int cc = 0; cc < 4; ++cc) {
-                        const int col_in_job = half * 128 + cc * 32;
-                        float gv[32];
-                        tc_ld32(tmem + ((uint32_t)(quad * 32) << 16) + (uint32_t)(acc * BN + col_in_job), gv);
-                        if (valid) {
-                            const int64_t j0 = (int64_t)nt * BN + col_in_job;
-                            const Vec<4>* xg = (const Vec<4>*)(xr + j0);
-                            const Vec<4>* xl = (const Vec<4>*)(xr + H + j0);
-                            Vec<4>* og = (Vec<4>*)(dxr + j0);
-                            Vec<4>* ol = (Vec<4>*)(dxr + H + j0);
 #pragma unroll
-                            for (int q = 0; q < 4; ++q) {
-                                const Vec<4> gw = xg[q], lw = xl[q];
-                                Vec<4> dgo, dlo;
+                for (int k = 0; k < CPJ; ++k) {
+                    const int cur = k & 1;
+                    // prefetch the next chunk of this row: (nt, k + 1), or (nt + 1, 0) after the last
+                    const bool last = (k + 1 == CPJ);
+                    if (valid && (!last || nt + 1 < NT)) {
+                        const int64_t jn = last ? (int64_t)(nt + 1) * BN : (int64_t)nt * BN + (k + 1) * CW;
 #pragma unroll
-                                for (int i = 0; i < 4; ++i) {
-                                    const float g0 = gv[q * 8 + 2 * i], g1 = gv[q * 8 + 2 * i + 1];
-                                    situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gw.w[i]), bf16_lo(lw.w[i]), pr16 * g0, c);
-                                    situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gw.w[i]), bf16_hi(lw.w[i]), pr16 * g1, c);
-                                    acc_dp = fmaf(g0, b0.a16, acc_dp);
-                                    acc_dp = fmaf(g1, b1.a16, acc_dp);
-                                    dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
-                                    dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
-                                }
-                                st_stream<4>(og + q, dgo);
-                                st_stream<4>(ol + q, dlo);
+                        for (int v = 0; v < XV; ++v) {
+                            xb[cur ^ 1][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + jn + 16 * v));
+                            xb[cur ^ 1][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn + 16 * v));
+                        }
+                    }
+                    float gv[CW];
+                    if (ok) tc_ld<CW>(tmem + t_lane + (uint32_t)(acc * BN + slot * COLS_PER_WARP + k * CW), gv);
+                    if (last) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->tempty[acc]);       // accumulator may be overwritten
+                    }
+                    if (ok && valid) {
+                        const int64_t j0 = (int64_t)nt * BN + k * CW;
+#pragma unroll
+                        for (int v = 0; v < XV; ++v) {
+                            Vec<8> dgo, dlo;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const uint32_t gw = xb[cur][0][v].w[i], lw = xb[cur][1][v].w[i];
+                                const float g0 = gv[16 * v + 2 * i], g1 = gv[16 * v + 2 * i + 1];
+                                situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gw), bf16_lo(lw), pr16 * g0, c);
+                                situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gw), bf16_hi(lw), pr16 * g1, c);
+                                acc_dp = fmaf(g0, b0.a16, acc_dp);
+                                acc_dp = fmaf(g1, b1.a16, acc_dp);
+                                dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
+                                dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
                             }
+                            st_stream<8>((Vec<8>*)(dxr + j0 + 16 * v), dgo);
+                            st_stream<8>((Vec<8>*)(dxr + H + j0 + 16 * v), dlo);
                         }
                     }
                 }
-                tc_fence_before();
-                mbar_arrive(&bars->tempty[acc]);               // accumulator may be overwritten
             }
-            // combine the two column halves of each row
-            if (half == 1) dp_half[lrow] = acc_dp;
+            // combine the EPW column slices of each row
+            if (slot > 0) dp_part[slot * BM + lrow] = acc_dp;
             epi_barrier();
-            if (half == 0 && valid) dp[row] = 16.0f * (acc_dp + dp_half[lrow]);
+            if (slot == 0 && valid) {
+                float s = acc_dp;
+#pragma unroll
+                for (int k = 1; k < EPW; ++k) s += dp_part[k * BM + lrow];
+                dp[row] = 16.0f * s;
+            }
             epi_barrier();
         }
     }
@@ -431,7 +474,7 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
     if (R > INT32_MAX || E * H > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
     if (R == 0) return SITU_GLU_OK;
     if (!x || !dy || !w_down_t || !expert_offsets || !p || !dx || !dp) return SITU_GLU_INVALID_ARG;
-    if (!aligned(x, 16) || !aligned(dy, 16) || !aligned(w_down_t, 16) || !aligned(dx, 16) ||
+    if (!aligned(x, 32) || !aligned(dy, 16) || !aligned(w_down_t, 16) || !aligned(dx, 32) ||
         !aligned(expert_offsets, 8) || !aligned(p, 4) || !aligned(dp, 4) || (status && !aligned(status, 4)))
         return SITU_GLU_INVALID_ARG;
     const Range rx = range_of(x, R * 2 * H * 2), ry = range_of(dy, R * D * 2), rw = range_of(w_down_t, E * H * D * 2);

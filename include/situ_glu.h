@@ -180,7 +180,8 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.
  *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 4096, R < 2^31, E*H < 2^31
- *   Pointers to x, dy, w_down_t, dx must be 16-byte aligned (TMA and vector access).
+ *   Pointers to dy and w_down_t must be 16-byte aligned (TMA), to x and dx 32-byte aligned
+ *   (32-byte vector access).
  * Returns SITU_GLU_INVALID_ARG for shapes or alignments outside these limits (there is no
  * general-shape fallback for this entry point).
  * --------------------------------------------------------------------------------------- */

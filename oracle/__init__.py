@@ -80,6 +80,12 @@ class Oracle:
         lib.oracle_quantize_fp8.restype = cint
         lib.oracle_dequantize_fp8.argtypes = [vp, vp, vp, i64, i64, i64]
         lib.oracle_dequantize_fp8.restype = cint
+        lib.oracle_round_bf16.argtypes = [dbl]
+        lib.oracle_round_bf16.restype = ctypes.c_uint16
+        lib.oracle_round_bf16_array.argtypes = [vp, vp, i64]
+        lib.oracle_round_bf16_array.restype = cint
+        lib.oracle_bf16_neighbours.argtypes = [dbl, vp, vp]
+        lib.oracle_bf16_neighbours.restype = None
         self.lib = lib
         self.path = path
 
@@ -184,6 +190,41 @@ class Oracle:
         g = (np.ascontiguousarray(g_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32)
         return self.bwd_router_f64(xh, g.astype(np.float64), np.asarray(p, dtype=np.float32).astype(np.float64),
                                    beta, lbeta, nthreads)
+
+
+    # ---------------- bf16 rounding of exact values ----------------
+
+    def round_bf16(self, v: float) -> int:
+        """bf16 bits of v rounded to nearest, ties to even (IEEE roundTiesToEven)."""
+        return int(self.lib.oracle_round_bf16(float(v)))
+
+    def round_bf16_array(self, v) -> np.ndarray:
+        v = np.ascontiguousarray(v, dtype=np.float64)
+        out = np.empty(v.shape, dtype=np.uint16)
+        _check(self.lib.oracle_round_bf16_array(_ptr(v), _ptr(out), v.size))
+        return out
+
+    def bf16_neighbours(self, v: float):
+        """(lo, hi) bf16 bits with lo <= v <= hi, consecutive or equal."""
+        lo = np.zeros(1, dtype=np.uint16)
+        hi = np.zeros(1, dtype=np.uint16)
+        self.lib.oracle_bf16_neighbours(float(v), _ptr(lo), _ptr(hi))
+        return int(lo[0]), int(hi[0])
+
+    # ---------------- fused gate/up projection forward ----------------
+
+    @staticmethod
+    def grouped_gateup(h_bits, w_bits, offsets):
+        return grouped_gateup(h_bits, w_bits, offsets)
+
+    def gateup_fwd(self, h_bits, w_bits, offsets, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+        """The gate/up projection with the SiTU-GLU forward after it: x (exact, double), its bf16
+        bits (rounded to nearest even: the saved tensor), out = G(gate)·L(linear) in double from
+        those bf16 values (the forward reads the saved bf16 x), and the accumulation scale of x."""
+        x, mag = grouped_gateup(h_bits, w_bits, offsets)
+        xb = self.round_bf16_array(x)
+        out = self.fwd_bf16(xb, beta, lbeta, nthreads)
+        return x, xb, out, mag
 
 
 def _ptr(a: np.ndarray) -> int:
@@ -311,3 +352,45 @@ def dgrad_bwd_router_rows(x_bits, dy_bits, experts, wt_of_expert, p, beta: float
             np.float32).astype(np.float64)
         g[rows] = dy[rows] @ wt.T
     return _default().bwd_router_f64(x, g, np.asarray(p, dtype=np.float32).astype(np.float64), beta, lbeta)
+
+
+# ---------------------------------------------------------------- fused gate/up projection forward
+
+def round_bf16(v: float) -> int:
+    return _default().round_bf16(v)
+
+
+def round_bf16_array(v) -> np.ndarray:
+    return _default().round_bf16_array(v)
+
+
+def bf16_neighbours(v: float):
+    return _default().bf16_neighbours(v)
+
+
+def grouped_gateup(h_bits, w_bits, offsets):
+    """x = [W_gate,e·h | W_up,e·h] per routed row, in double: rows offsets[e]..offsets[e+1] of
+    h (bf16 bits [R, D], the expert's dispatched inputs) times expert e's stacked weights
+    w_bits[e] (bf16 bits [2H, D]: rows 0..H-1 are W_gate,e, rows H..2H-1 are W_up,e), so
+    x[r, n] = Σ_d h[r, d]·w[e, n, d]. Also returns Σ_d |h[r, d]·w[e, n, d]|, the scale of the
+    fp32 accumulation error of any summation order.
+
+    "Kimi K3 模型结构（9）：显存", section "MoE 反向…": a_e = SiTU(W_gate,e x_e, W_up,e x_e);
+    the two projections are formed here with numpy's fp64 matmul."""
+    h = (np.ascontiguousarray(h_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    w = (np.ascontiguousarray(w_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E, H2, D = w.shape
+    assert h.shape[1] == D and offsets.shape == (E + 1,) and offsets[0] == 0 and offsets[-1] == h.shape[0]
+    x = np.zeros((h.shape[0], H2), dtype=np.float64)
+    mag = np.zeros((h.shape[0], H2), dtype=np.float64)
+    for e in range(E):
+        a, b = int(offsets[e]), int(offsets[e + 1])
+        if b > a:
+            x[a:b] = h[a:b] @ w[e].T
+            mag[a:b] = np.abs(h[a:b]) @ np.abs(w[e]).T
+    return x, mag
+
+
+def gateup_fwd(h_bits, w_bits, offsets, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
+    return _default().gateup_fwd(h_bits, w_bits, offsets, beta, lbeta, nthreads)

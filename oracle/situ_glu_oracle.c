@@ -373,3 +373,70 @@ int oracle_dequantize_fp8(const uint8_t* q, const float* s, float* xhat, int64_t
     }
     return 0;
 }
+
+/* ===================================================================================
+ * bf16 rounding of an exact (double) value, for the gate/up projection whose output x is
+ * saved in bf16 ([K3-RL] "Streaming activations": x is "the bf16 input tensor"; [K3-MEM]
+ * section "MoE 反向…": x_e's two halves are W_gate,e·x_e and W_up,e·x_e). bf16 has 8
+ * significant bits, exponents -126..127, subnormals down to 2^-133 and a largest finite value
+ * (2 - 2^-7)·2^127. Rounding is to nearest, ties to the even significand (IEEE 754
+ * roundTiesToEven), overflowing to infinity exactly when the rounded magnitude would need
+ * exponent 128.
+ * =================================================================================== */
+
+/* Bits of a bf16 value given exactly as a double (an exact float, so its top 16 bits). */
+static uint16_t bf16_bits_of_exact(double r) {
+    float f = (float)r;
+    uint32_t u;
+    memcpy(&u, &f, 4);
+    return (uint16_t)(u >> 16);
+}
+
+/* The two bf16 values bracketing v: *lo <= v <= *hi, consecutive (or equal when v is a bf16
+ * value). Finite v only; magnitudes beyond the largest finite bf16 bracket with infinity. */
+void oracle_bf16_neighbours(double v, uint16_t* lo, uint16_t* hi) {
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);                          /* a = m·2^e, m in [0.5, 1) */
+    int ex = (a == 0.0) ? -126 : e - 1;    /* a in [2^ex, 2^(ex+1)) */
+    if (ex < -126) ex = -126;              /* subnormal range: spacing 2^-133 */
+    double ulp = ldexp(1.0, ex - 7);
+    double q = floor(a / ulp);             /* a / ulp is exact (power-of-two scaling) */
+    double dn = q * ulp, up = (q * ulp == a) ? a : (q + 1.0) * ulp;
+    const double maxf = ldexp(255.0, 120); /* (2 - 2^-7)·2^127 */
+    uint16_t bdn = dn > maxf ? 0x7F80 : bf16_bits_of_exact(dn);
+    uint16_t bup = up > maxf ? 0x7F80 : bf16_bits_of_exact(up);
+    if (v < 0.0 || (v == 0.0 && signbit(v))) {
+        *lo = (uint16_t)(bup | 0x8000);
+        *hi = (uint16_t)(bdn | 0x8000);
+    } else {
+        *lo = bdn;
+        *hi = bup;
+    }
+}
+
+/* v rounded to the nearest bf16, ties to even; NaN -> the canonical quiet NaN 0x7FC0,
+ * +-infinity kept, signed zero kept. */
+uint16_t oracle_round_bf16(double v) {
+    if (isnan(v)) return 0x7FC0;
+    if (isinf(v)) return v > 0 ? 0x7F80 : 0xFF80;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);
+    int ex = (a == 0.0) ? -126 : e - 1;
+    if (ex < -126) ex = -126;
+    double ulp = ldexp(1.0, ex - 7);
+    double q = a / ulp;                    /* exact */
+    double fl = floor(q), rem = q - fl;    /* rem exact */
+    double n = fl;
+    if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) n = fl + 1.0;
+    double r = n * ulp;
+    uint16_t b = r > ldexp(255.0, 120) ? 0x7F80 : bf16_bits_of_exact(r);
+    return (uint16_t)((signbit(v) ? 0x8000 : 0) | b);
+}
+
+int oracle_round_bf16_array(const double* v, uint16_t* out, int64_t n) {
+    if (n < 0) return 1;
+    for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(v[i]);
+    return 0;
+}

@@ -442,3 +442,82 @@ def pin_grouped_dgrad(o_mod):
             o_e = wtf[e].T @ a[r]                          # o_e = W_down,e · a_e  (W_down,e = wt[e]ᵀ)
             naive = float(dyf[r] @ o_e)                    # <dL/dy, o_e>
             assert abs(dp[r] - naive) <= 1e-12 * max(1.0, abs(naive))
+
+
+# ---------------------------------------------------------------- bf16 rounding, gate/up projection
+
+def pin_round_bf16(o):
+    """Round-to-nearest-even from double to bf16, against what fixes it independently:
+    - for doubles that are exact fp32 values, PyTorch's fp32 -> bf16 cast (RNE) on 40000 random
+      finite bit patterns (normals, subnormals, both signs) plus signed zeros and the extremes;
+    - exact midpoints between consecutive bf16 values go to the even significand, and the
+      nearest double on either side of a midpoint goes to the nearer value (this is where a
+      double -> fp32 -> bf16 double rounding would differ);
+    - overflow: the largest finite bf16 plus half its spacing rounds to infinity, anything
+      below that midpoint to the largest finite value; NaN stays NaN;
+    - bf16_neighbours brackets v with consecutive values and contains the rounded value."""
+    rng = np.random.default_rng(21)
+    bits = rng.integers(0, 2 ** 32, 40000, dtype=np.uint64).astype(np.uint32)
+    f = bits.view(np.float32)
+    f = f[np.isfinite(f)]
+    f = np.concatenate([f, np.array([0.0, -0.0, 1.0, -1.0, 3.3895313892515355e38, -3.3895313892515355e38,
+                                     1e-45, -1e-45, 2.0 ** -133, 2.0 ** -126, 65504.0], dtype=np.float32)])
+    want = torch.from_numpy(f).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got = o.round_bf16_array(f.astype(np.float64))
+    assert np.array_equal(got, want)
+    # midpoints and their neighbours, across binades and in the subnormal range
+    for b in [0x3F80, 0x3F81, 0x4049, 0x0001, 0x0002, 0x007F, 0x0080, 0x7F7E, 0xBF80, 0xBF81, 0x8001]:
+        lo = o.bf16_to_double(b)
+        hi = o.bf16_to_double(b + 1)
+        mid = (lo + hi) / 2.0                                  # exact in double
+        even = b if (b & 1) == 0 else b + 1
+        assert o.round_bf16(mid) == even, hex(b)
+        toward_hi = math.nextafter(mid, hi)
+        toward_lo = math.nextafter(mid, lo)
+        assert o.round_bf16(toward_hi) == b + 1 and o.round_bf16(toward_lo) == b, hex(b)
+    maxf = o.bf16_to_double(0x7F7F)
+    half = 2.0 ** 119                                          # half the spacing at the top binade
+    assert o.round_bf16(maxf + half) == 0x7F80
+    assert o.round_bf16(math.nextafter(maxf + half, 0.0)) == 0x7F7F
+    assert o.round_bf16(-(maxf + half)) == 0xFF80
+    assert o.round_bf16(float("inf")) == 0x7F80 and o.round_bf16(float("-inf")) == 0xFF80
+    assert (o.round_bf16(float("nan")) & 0x7FFF) > 0x7F80
+    assert o.round_bf16(-0.0) == 0x8000 and o.round_bf16(0.0) == 0x0000
+    for v in [1.001, -1.001, 2.0 ** -130 * 1.3, 1e30, -7.77e-3, 3.0, 0.0]:
+        lo, hi = o.bf16_neighbours(v)
+        dlo, dhi = o.bf16_to_double(lo), o.bf16_to_double(hi)
+        assert dlo <= v <= dhi
+        r = o.round_bf16(v)
+        assert r in (lo, hi)
+        if dlo != dhi:
+            assert abs(int(hi) - int(lo)) == 1                 # consecutive bf16 values
+
+
+def pin_grouped_gateup(o):
+    """The oracle's gate/up projection equals a brute-force triple loop (experts with 0 rows
+    included), puts W_gate,e·h in columns 0..H-1 and W_up,e·h in H..2H-1, and its out is
+    SiTU(gate, linear) of the bf16-rounded projections, element by element through the
+    oracle's point function (a_e = SiTU(W_gate,e x_e, W_up,e x_e))."""
+    rng = np.random.default_rng(13)
+    E, H, D = 4, 3, 5
+    counts = [2, 0, 3, 1]
+    off = np.concatenate([[0], np.cumsum(counts)])
+    R = int(off[-1])
+    h = _bf16_bits(rng.normal(0, 1, (R, D)))
+    w = _bf16_bits(rng.normal(0, 1.5, (E * 2 * H, D))).reshape(E, 2 * H, D)
+    x, mag = o.grouped_gateup(h, w, off)
+    x2, xb, out, mag2 = o.gateup_fwd(h, w, off)
+    hf, wf = _bits_to_f32(h).astype(np.float64), _bits_to_f32(w).astype(np.float64)
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            for n in range(2 * H):
+                ref = sum(hf[r, d] * wf[e, n, d] for d in range(D))
+                refa = sum(abs(hf[r, d] * wf[e, n, d]) for d in range(D))
+                assert abs(x[r, n] - ref) <= 1e-12 * max(1.0, abs(ref))
+                assert abs(mag[r, n] - refa) <= 1e-12 * max(1.0, refa)
+                assert xb[r, n] == o.round_bf16(ref)
+            for j in range(H):
+                u, v = o.bf16_to_double(int(xb[r, j])), o.bf16_to_double(int(xb[r, H + j]))
+                G, L, _, _ = o.point(u, v)
+                assert abs(out[r, j] - G * L) <= 1e-14 * max(1.0, abs(G * L))
+    assert np.array_equal(x, x2) and np.array_equal(mag, mag2)

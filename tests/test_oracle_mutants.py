@@ -27,6 +27,8 @@ PINS = [
     ("e4m3_codec", _pins.pin_e4m3_codec),
     ("fp8_blocks", _pins.pin_fp8_block_quantization),
     ("fp8_bwd", _pins.pin_fp8_backward_is_backward_of_dequantized),
+    ("round_bf16", _pins.pin_round_bf16),
+    ("gateup", _pins.pin_grouped_gateup),
 ]
 
 MUTANTS = {
@@ -63,6 +65,16 @@ MUTANTS = {
     "fp8_linear_scales_overwrite_gate": ("s + r * 2 * nb + nb, block);", "s + r * 2 * nb, block);"),
     "fp8_dequant_ignores_half": ("float sc = s[r * 2 * nb + half * nb + j / block];",
                                  "float sc = s[r * 2 * nb + j / block];"),
+    # bf16 rounding of the gate/up projection
+    "bf16_ties_away": ("if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) n = fl + 1.0;",
+                       "if (rem >= 0.5) n = fl + 1.0;"),
+    "bf16_truncates": ("if (rem > 0.5 || (rem == 0.5 && fmod(fl, 2.0) != 0.0)) n = fl + 1.0;", "(void)rem;"),
+    "bf16_seven_bits": ("    double ulp = ldexp(1.0, ex - 7);\n    double q = a / ulp;",
+                        "    double ulp = ldexp(1.0, ex - 6);\n    double q = a / ulp;"),
+    "bf16_no_subnormal_clamp": ("    if (ex < -126) ex = -126;\n    double ulp = ldexp(1.0, ex - 7);\n    double q = a / ulp;",
+                                "    double ulp = ldexp(1.0, ex - 7);\n    double q = a / ulp;"),
+    "bf16_overflow_at_max": ("uint16_t b = r > ldexp(255.0, 120) ? 0x7F80", "uint16_t b = r >= ldexp(255.0, 120) ? 0x7F80"),
+    "bf16_sign_dropped": ("return (uint16_t)((signbit(v) ? 0x8000 : 0) | b);", "return b;"),
 }
 
 

@@ -92,3 +92,11 @@ def test_fp8_backward_is_backward_of_dequantized():
 
 def test_grouped_dgrad():
     _pins.pin_grouped_dgrad(oracle)
+
+
+def test_round_bf16():
+    _pins.pin_round_bf16(oracle)
+
+
+def test_grouped_gateup():
+    _pins.pin_grouped_gateup(oracle)
