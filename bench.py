@@ -65,9 +65,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 saved-x variant's timing")
     ap.add_argument("--no-dgrad", action="store_true", help="skip the fused dgrad GEMM's timing")
+    ap.add_argument("--no-gateup", action="store_true", help="skip the fused gate/up GEMM's timing")
     ap.add_argument("--only-dgrad", action="store_true", help="time only the fused dgrad GEMM (profiling runs)")
-    ap.add_argument("--dgrad-rows", type=int, default=None, help="rows split evenly over --dgrad-experts")
-    ap.add_argument("--dgrad-experts", type=int, default=None)
+    ap.add_argument("--only-gateup", action="store_true", help="time only the fused gate/up GEMM (profiling runs)")
+    ap.add_argument("--gemm-rows", type=int, default=None, help="rows split evenly over --gemm-experts")
+    ap.add_argument("--gemm-experts", type=int, default=None)
     ap.add_argument("--rows", type=int, default=None, help="override R (for small profiling runs)")
     return ap.parse_args(argv)
 
@@ -264,7 +266,8 @@ def run_reference(args):
 
 # ---------------------------------------------------------------- native arm
 
-def run_dgrad_only(args):
+def run_gemm_only(args):
+    """Time only the fused tensor-core kernels (profiling runs)."""
     import torch
 
     import bwd_situ_glu_gb300 as sg
@@ -273,9 +276,17 @@ def run_dgrad_only(args):
     sg.build()
     sg.load()
     peak, _ = load_peaks()
-    res = time_dgrad(sg, dev, args.steps, args.warmup, peak, rows=args.dgrad_rows, experts=args.dgrad_experts)
-    print(json.dumps({"dgrad_fused": res}), flush=True)
-    return 0 if res["status"] == 0 else 1
+    line, ok = {}, True
+    if args.only_dgrad:
+        line["dgrad_fused"] = time_dgrad(sg, dev, args.steps, args.warmup, peak, rows=args.gemm_rows,
+                                         experts=args.gemm_experts)
+        ok &= line["dgrad_fused"]["status"] == 0
+    if args.only_gateup:
+        line["gateup_fused"] = time_gateup(sg, dev, args.steps, args.warmup, peak, rows=args.gemm_rows,
+                                           experts=args.gemm_experts)
+        ok &= line["gateup_fused"]["status"] == 0
+    print(json.dumps(line), flush=True)
+    return 0 if ok else 1
 
 
 def run_native(args):
@@ -359,6 +370,7 @@ def run_native(args):
 
     fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
     dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak)
+    gateup = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak)
 
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_hash() and NCU_TRAFFIC["bwd_bytes_per_row"]:
@@ -413,6 +425,7 @@ def run_native(args):
         "cpu_baseline": cpu,
         "fp8_saved_x": fp8,
         "dgrad_fused": dgrad,
+        "gateup_fused": gateup,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -463,72 +476,121 @@ def time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, warmup, peak):
             "gpu_launches": 2 * steps}
 
 
-def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, experts=None):
-    """Fused down-projection dgrad (tcgen05 grouped GEMM) + backward + router gradient on the
-    expert-grouped workload: 16384 tokens x top-16 of 896 experts, rows grouped by expert,
-    H = 3072, D = 3584 (the expert output width), synthetic N(0, 1/D) weights.
-    With rows and experts given: that many rows split evenly over that many experts instead."""
+def grouped_workload(seed, rows=None, experts=None):
+    """Expert-grouped routed rows: 16384 tokens x top-16 of 896 experts, rows sorted by expert
+    (H = 3072), or with rows and experts given, that many rows split evenly over that many
+    experts. Returns (counts per expert, router weights p [R] on the CPU, workload name, H)."""
     import numpy as np
     import torch
 
     import situ_inputs as si
     w = si.get("expert_grouped_r262144_h3072")
     if rows and experts:
-        E = experts
-        counts = np.full(E, rows // E, dtype=np.int64)
-        counts[: rows % E] += 1
+        counts = np.full(experts, rows // experts, dtype=np.int64)
+        counts[: rows % experts] += 1
         p = torch.rand(rows, generator=torch.Generator().manual_seed(seed))
-        R, H = rows, w.H
-        workload = f"uniform_r{rows}_e{E}_h{H}_d{D}"
-    else:
-        p, experts_of_row, _ = si.router_rows(w.tokens, w.seed, order="expert")
-        counts = np.bincount(experts_of_row.numpy(), minlength=si.N_EXPERTS)
-        R, H, E = w.R, w.H, si.N_EXPERTS
-        workload = f"expert_grouped_r{R}_h{H} x D={D}, {E} experts"
+        return counts, p, f"uniform_r{rows}_e{experts}_h{w.H}", w.H, w.x_std
+    p, experts_of_row, _ = si.router_rows(w.tokens, w.seed, order="expert")
+    counts = np.bincount(experts_of_row.numpy(), minlength=si.N_EXPERTS)
+    return counts, p, f"expert_grouped_r{w.R}_h{w.H}, {si.N_EXPERTS} experts", w.H, w.x_std
+
+
+def bf16_tflops_peak():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+def randn_bf16(shape, gen, dev, scale=1.0, chunk=1 << 27):
+    """Seeded N(0, scale²) bf16 tensor, generated on the device in chunks of `chunk` elements."""
+    import torch
+    t = torch.empty(shape, dtype=torch.bfloat16, device=dev)
+    flat = t.view(-1)
+    for a in range(0, flat.numel(), chunk):
+        b = min(flat.numel(), a + chunk)
+        flat[a:b] = (torch.randn(b - a, generator=gen, device=dev) * scale).to(torch.bfloat16)
+    return t
+
+
+def time_launches(fn, stream, steps, warmup):
+    """Average ms per launch of fn over `steps` back-to-back launches on `stream` (CUDA events),
+    after `warmup` untimed ones."""
+    import torch
+    for _ in range(max(1, warmup)):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def gemm_result(workload, ms, flops, nbytes, hbm_peak, steps, status):
+    tf_peak, tf_src = bf16_tflops_peak()
+    t_flop = flops / (tf_peak * 1e12) * 1e3
+    t_byte = nbytes / (hbm_peak * 1e9) * 1e3
+    return {"workload": workload,
+            "ms": ms, "TFLOP_s": flops / ms / 1e9, "frac_of_bf16_peak": flops / ms / 1e9 / tf_peak,
+            "bf16_peak": tf_peak, "bf16_peak_source": tf_src,
+            "GB_s": nbytes / ms / 1e6, "frac_of_hbm_peak": nbytes / ms / 1e6 / hbm_peak,
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+            "bound": "tensor" if t_flop >= t_byte else "hbm",
+            "roofline_frac": max(t_flop, t_byte) / ms, "status": status, "gpu_launches": steps}
+
+
+def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, experts=None):
+    """Fused down-projection dgrad (tcgen05 grouped GEMM) + backward + router gradient on the
+    expert-grouped workload, D = 3584 (the expert output width), synthetic N(0, 1/D) weights."""
+    import numpy as np
+    import torch
+    counts, p, workload, H, x_std = grouped_workload(seed, rows, experts)
+    R, E = int(counts.sum()), len(counts)
     gen = torch.Generator(device=dev).manual_seed(seed)
-    x = (torch.randn(R, 2 * H, generator=gen, device=dev) * w.x_std).to(torch.bfloat16)
-    dy = torch.empty(R, D, dtype=torch.bfloat16, device=dev)
-    for a in range(0, R, 32768):
-        dy[a:a + 32768] = torch.randn(min(32768, R - a), D, generator=gen, device=dev).to(torch.bfloat16)
-    wt = torch.empty(E, H, D, dtype=torch.bfloat16, device=dev)
-    for e in range(E):
-        wt[e] = (torch.randn(H, D, generator=gen, device=dev) / D ** 0.5).to(torch.bfloat16)
+    x = randn_bf16((R, 2 * H), gen, dev, x_std)
+    dy = randn_bf16((R, D), gen, dev)
+    wt = randn_bf16((E, H, D), gen, dev, 1.0 / D ** 0.5)
     off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=dev)
     p = p.to(dev)
     dx = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
     dp = torch.empty(R, dtype=torch.float32, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    for _ in range(max(1, warmup)):
-        sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx, dp, status=status)
-    torch.cuda.synchronize(dev)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(steps):
-        sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx, dp, status=status)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    ms = e0.elapsed_time(e1) / steps
-    flops = 2.0 * R * D * H
+    ms = time_launches(lambda: sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx, dp, status=status),
+                       stream, steps, warmup)
     nbytes = R * D * 2 + E * H * D * 2 + R * 4 * H + R * 4 * H + R * 8 + (E + 1) * 8
-    tf_peak = None
-    try:
-        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
-            tf_peak = float(json.load(f)["bf16_tflops"])
-    except (OSError, KeyError, ValueError):
-        tf_peak = 1900.0
-    t_flop = flops / (tf_peak * 1e12) * 1e3
-    t_byte = nbytes / (hbm_peak * 1e9) * 1e3
-    bound = "tensor" if t_flop >= t_byte else "hbm"
+    res = gemm_result(f"{workload} x D={D}", ms, 2.0 * R * D * H, nbytes, hbm_peak, steps, int(status.item()))
     del x, dy, wt, dx, dp
     torch.cuda.empty_cache()
-    return {"workload": workload,
-            "ms": ms, "TFLOP_s": flops / ms / 1e9, "frac_of_bf16_peak": flops / ms / 1e9 / tf_peak,
-            "GB_s": nbytes / ms / 1e6, "frac_of_hbm_peak": nbytes / ms / 1e6 / hbm_peak,
-            "algorithmic_flops": flops, "algorithmic_bytes": nbytes, "bound": bound,
-            "roofline_frac": max(t_flop, t_byte) / ms, "status": int(status.item()),
-            "gpu_launches": steps}
+    return res
+
+
+def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, experts=None):
+    """Fused gate/up projection (tcgen05 grouped GEMM, N = 2H) + SiTU-GLU forward on the
+    expert-grouped workload: h [R, D] ~ N(0, 1), [W_gate; W_up] ~ N(0, x_std²/D) per expert."""
+    import numpy as np
+    import torch
+    counts, _, workload, H, x_std = grouped_workload(seed, rows, experts)
+    R, E = int(counts.sum()), len(counts)
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    h = randn_bf16((R, D), gen, dev)
+    w = randn_bf16((E, 2 * H, D), gen, dev, x_std / D ** 0.5)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=dev)
+    x = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
+    out = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ms = time_launches(lambda: sg.situ_glu_fwd_gateup(h, w, off, x, out, status=status), stream, steps, warmup)
+    nbytes = R * D * 2 + E * 2 * H * D * 2 + R * 4 * H + R * 2 * H + (E + 1) * 8
+    res = gemm_result(f"{workload} x D={D}", ms, 2.0 * R * D * 2 * H, nbytes, hbm_peak, steps, int(status.item()))
+    del h, w, x, out
+    torch.cuda.empty_cache()
+    return res
 
 
 def pinned_like(t):
@@ -632,8 +694,8 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
-    if args.only_dgrad:
-        return run_dgrad_only(args)
+    if args.only_dgrad or args.only_gateup:
+        return run_gemm_only(args)
     return run_native(args)
 
 

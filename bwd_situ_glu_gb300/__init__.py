@@ -28,10 +28,10 @@ CSRC = os.path.join(_HERE, "csrc")
 INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
-SOURCES = [os.path.join(CSRC, "situ_glu.cu"), os.path.join(CSRC, "situ_glu_fp8.cu"),
-           os.path.join(CSRC, "situ_glu_dgrad.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h")] + [
-    os.path.join(INCLUDE, "situ_glu.h")]
+SOURCES = [os.path.join(CSRC, n) for n in ("situ_glu.cu", "situ_glu_fp8.cu", "situ_glu_dgrad.cu",
+                                             "situ_glu_gateup.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h",
+                                                     "situ_tc.cuh")] + [os.path.join(INCLUDE, "situ_glu.h")]
 
 NVCC_FLAGS = [
     "-std=c++17", "-O3", "-lineinfo",
@@ -63,12 +63,27 @@ def build(force: bool = False, verbose: bool = False) -> str:
         os.makedirs(LIB_DIR, exist_ok=True)
         newest = max(os.path.getmtime(p) for p in DEPENDS)
         if force or not os.path.exists(LIB_PATH) or os.path.getmtime(LIB_PATH) < newest:
-            tmp = LIB_PATH + f".tmp{os.getpid()}"
-            cmd = [_nvcc(), *NVCC_FLAGS, "-I", INCLUDE, "-o", tmp, *SOURCES]
-            if verbose:
-                cmd.insert(1, "-Xptxas=-v")
-            subprocess.run(cmd, check=True)
-            os.replace(tmp, LIB_PATH)
+            # one object per translation unit, compiled in parallel, then one link
+            tag = f".tmp{os.getpid()}"
+            objs, procs = [], []
+            for src in SOURCES:
+                obj = os.path.join(LIB_DIR, os.path.basename(src) + tag + ".o")
+                cmd = [_nvcc(), *[f for f in NVCC_FLAGS if f != "-shared"], "-I", INCLUDE, "-c", "-o", obj, src]
+                if verbose:
+                    cmd.insert(1, "-Xptxas=-v")
+                objs.append(obj)
+                procs.append((subprocess.Popen(cmd), cmd))
+            failed = [cmd for proc, cmd in procs if proc.wait() != 0]
+            try:
+                if failed:
+                    raise subprocess.CalledProcessError(1, failed[0])
+                tmp = LIB_PATH + tag
+                subprocess.run([_nvcc(), *NVCC_FLAGS, "-o", tmp, *objs], check=True)
+                os.replace(tmp, LIB_PATH)
+            finally:
+                for obj in objs:
+                    if os.path.exists(obj):
+                        os.remove(obj)
     return LIB_PATH
 
 
@@ -91,6 +106,8 @@ def load():
     lib.situ_glu_bwd_router_fp8.restype = cint
     lib.situ_glu_bwd_router_dgrad.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp]
     lib.situ_glu_bwd_router_dgrad.restype = cint
+    lib.situ_glu_fwd_gateup.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, f32, f32, vp]
+    lib.situ_glu_fwd_gateup.restype = cint
     lib.situ_glu_status_string.argtypes = [cint]
     lib.situ_glu_status_string.restype = ctypes.c_char_p
     lib.situ_glu_last_cuda_error.argtypes = []
@@ -284,10 +301,43 @@ def situ_glu_bwd_router_dgrad(x, dy, w_down_t, expert_offsets, p, dx=None, dp=No
     return dx, dp
 
 
+def situ_glu_fwd_gateup(h, w_gate_up, expert_offsets, x=None, out=None, status=None, beta: float = 4.0,
+                        lbeta: float = 25.0, stream=None):
+    """(x bf16 [R,2H], out bf16 [R,H]) from the dispatched inputs h [R,D] and the experts' stacked
+    [W_gate; W_up] [E,2H,D]: the gate/up GEMM on the tensor cores with the forward fused into it
+    (x is the bf16-rounded projection, out the forward of that x).
+    ``status`` (int32 [1] on the device, zeroed by the caller) turns 1 if a pipeline wait timed out."""
+    import torch
+    if h.dim() != 2:
+        raise ValueError("h must be [R, D]")
+    if w_gate_up.dim() != 3 or w_gate_up.shape[1] % 2 != 0:
+        raise ValueError("w_gate_up must be [E, 2H, D]")
+    R, D = h.shape
+    E, H = w_gate_up.shape[0], w_gate_up.shape[1] // 2
+    _need(h, torch.bfloat16, (R, D), "h")
+    _need(w_gate_up, torch.bfloat16, (E, 2 * H, D), "w_gate_up")
+    _need(expert_offsets, torch.int64, (E + 1,), "expert_offsets")
+    if x is None:
+        x = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=h.device)
+    if out is None:
+        out = torch.empty((R, H), dtype=torch.bfloat16, device=h.device)
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    _need(out, torch.bfloat16, (R, H), "out")
+    sptr = 0
+    if status is not None:
+        _need(status, torch.int32, (1,), "status")
+        sptr = status.data_ptr()
+    with torch.cuda.device(h.device):
+        _check(load().situ_glu_fwd_gateup(h.data_ptr(), w_gate_up.data_ptr(), expert_offsets.data_ptr(), E,
+                                          x.data_ptr(), out.data_ptr(), sptr, R, H, D, beta, lbeta,
+                                          _stream_handle(stream, h.device)))
+    return x, out
+
+
 __all__ = [
     "build", "load", "version", "status_string", "SituGluError",
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
-    "situ_glu_bwd_router_dgrad",
+    "situ_glu_bwd_router_dgrad", "situ_glu_fwd_gateup",
     "LIB_PATH", "INCLUDE",
 ]

@@ -9,18 +9,13 @@
 // from the fp32 accumulators and the saved bf16 x ("Frontier-scale RL with Kimi K3", section
 // "Streaming activations": the backward keeps only x and recomputes tanh and sigmoid).
 //
-// Per-CTA pipeline (one CTA per SM, persistent over M-tiles of 128 rows of one expert):
-//   warp 0      TMA producer: dY tile [128 x 64] and W_downᵀ tile [256 x 64] (bf16, 128-byte
-//               swizzle) into a 4-stage shared-memory ring, completion on mbarriers;
-//   warp 1      allocates 512 TMEM columns (two 128 x 256 fp32 accumulators) and one thread
-//               issues tcgen05.mma (M = 128, N = 256, K = 16), committing to mbarriers that free
-//               ring stages and hand finished accumulators to the epilogue;
-//   warps 2..   epilogue, EPW warps per 32-lane TMEM quadrant, each with a slice of the 256 columns;
-//               a thread owns one row, reads its g with tcgen05.ld, loads the matching x (prefetched
-//               one chunk ahead), and writes dx; its dp partial stays in a register across the
-//               N-tiles of the row.
-// Every mbarrier wait is bounded: on a timeout the CTA records a non-zero status, stops issuing,
-// drains what it issued, frees TMEM and returns.
+// The GEMM pipeline (persistent CTAs over 128-row M-tiles of one expert, TMA producer warp,
+// single-thread tcgen05.mma issuer, two TMEM accumulators, bounded mbarrier waits) is the one in
+// situ_tc.cuh, with A = dY and B = W_downᵀ (rows e·H + nt·256 ..). The epilogue here:
+//   EPW warps per 32-lane TMEM quadrant, each with a slice of the 256 columns of a job; a thread
+//   owns one row, reads its g with tcgen05.ld, loads the matching x (prefetched one chunk ahead,
+//   32-byte loads), and writes dx; its dp partial stays in a register across the N-tiles of the
+//   row and the EPW partials of a row are summed through shared memory at the end of the M-tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -30,20 +25,14 @@
 #include "situ_device.cuh"
 #include "situ_host.h"
 #include "situ_math.cuh"
+#include "situ_tc.cuh"
 
 namespace {
 
 using namespace situ;
 using namespace situ_host;
+using namespace situ_tc;
 
-constexpr int BM = 128;                      // rows per tile (TMEM lanes)
-constexpr int BN = 256;                      // accumulator columns per job
-constexpr int BK = 64;                       // K per ring stage (128 bytes of bf16: one swizzle row)
-constexpr int UK = 16;                       // K per tcgen05.mma (kind::f16)
-constexpr int STAGES = 4;
-constexpr int A_BYTES = BM * BK * 2;         // 16 KB
-constexpr int B_BYTES = BN * BK * 2;         // 32 KB
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int EPW = 2;                       // epilogue warps per 32-lane TMEM quadrant
 constexpr int CW = 32;                       // accumulator columns per tcgen05.ld chunk
 constexpr int NUM_EPI_THREADS = 4 * EPW * 32;
@@ -52,144 +41,10 @@ constexpr int COLS_PER_WARP = BN / EPW;      // accumulator columns of one job a
 constexpr int CPJ = COLS_PER_WARP / CW;      // chunks per job per epilogue warp
 constexpr int XV = CW / 16;                  // 32-byte vectors (16 bf16) per half-row per chunk
 static_assert(CPJ >= 2 && CPJ % 2 == 0, "the x prefetch alternates two register buffers");
-constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 columns
-constexpr int MAX_EXPERTS = 4096;
-constexpr uint32_t WAIT_LIMIT = 1u << 22;    // polls of a try_wait before giving up (~1-2 s)
-
-// Shared memory layout (dynamic, base rounded up to 1024 bytes for the 128-byte swizzle).
-struct alignas(8) Barriers {
-    uint64_t full[STAGES];
-    uint64_t empty[STAGES];
-    uint64_t tfull[2];
-    uint64_t tempty[2];
-    uint64_t mma_done;
-    uint32_t tmem_base;
-    int abort;
-};
-constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Barriers) + EPW * BM * 4 +
-                           (MAX_EXPERTS + 1) * 4 + 64;
-
-// ---------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
-
-__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(smem_addr(b)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// Bounded wait; on a timeout sets the CTA's abort flag and the caller's status word.
-__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Barriers* bars, int* status) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
-        if (mbar_try_wait(b, parity)) return true;
-        if (i > 64 && *(volatile int*)&bars->abort) return false;
-    }
-    *(volatile int*)&bars->abort = 1;
-    if (status) atomicExch(status, 1);
-    return false;
-}
-
-__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
-            smem_addr(dst)),
-        "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
-__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
-
-// Shared-memory matrix descriptor of a K-major bf16 tile with 128-byte swizzle: rows of 128 bytes,
-// 8-row groups 1024 bytes apart (stride byte offset), version bits 46-47 = 1, swizzle mode 2.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
-    uint64_t d = 0;
-    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
-    d |= (uint64_t)1 << 16;                           // leading byte offset (unused for swizzled K-major)
-    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
-    d |= (uint64_t)1 << 46;                           // descriptor version
-    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
-    return d;
-}
-
-// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, N = 256, M = 128.
-constexpr uint32_t IDESC = (1u << 4)           // D format fp32
-                         | (1u << 7)           // A format bf16
-                         | (1u << 10)          // B format bf16
-                         | ((uint32_t)(BN >> 3) << 17)
-                         | ((uint32_t)(BM >> 4) << 24);
-
-__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
-            d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
-                 : "memory");
-}
-
-// N consecutive fp32 columns (N = 16 or 32) of this thread's TMEM lane, waited for.
-template <int N>
-__device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[N]) {
-    uint32_t r[N];
-    if constexpr (N == 32) {
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
-            "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
-              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
-              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
-              "=r"(r[30]), "=r"(r[31])
-            : "r"(taddr));
-    } else {
-        static_assert(N == 16, "16 or 32 columns");
-        asm volatile(
-            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-            : "r"(taddr));
-    }
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-#pragma unroll
-    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-__device__ __forceinline__ void epi_barrier() { asm volatile("bar.sync 1, %0;" ::"r"(NUM_EPI_THREADS) : "memory"); }
-
-// M-tile t -> (expert, first row, end row of the expert).
-__device__ __forceinline__ void tile_rows(const int* tile_start, const int64_t* off, int E, int64_t R, int t,
-                                          int& e, int64_t& row0, int64_t& row_end) {
-    int lo = 0, hi = E - 1;                 // last e with tile_start[e] <= t
-    while (lo < hi) {
-        const int mid = (lo + hi + 1) >> 1;
-        if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
-    }
-    e = lo;
-    row0 = off[e] + (int64_t)(t - tile_start[e]) * BM;
-    row_end = off[e + 1] < R ? off[e + 1] : R;     // clamped: malformed offsets never index past R
-}
+constexpr int MAX_SPLIT = 8;                 // largest cluster (portable size)
+constexpr int DGRAD_SPLIT = 4;               // CTAs per cluster sharing an M-tile (each every 4th N-tile)
+// extra shared memory: dp_part [EPW][BM] | dp_cl [2][MAX_SPLIT][BM] | dp_full[2], dp_free[2]
+constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 16 + EPW * BM * 4 + 2 * MAX_SPLIT * BM * 4 + 4 * 8;
 
 // ---------------------------------------------------------------- the kernel
 
@@ -198,137 +53,41 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     dgrad_bwd_kernel(const __grid_constant__ CUtensorMap map_dy, const __grid_constant__ CUtensorMap map_w,
                      const uint16_t* __restrict__ x, const int64_t* __restrict__ offsets, const float* __restrict__ p,
                      uint16_t* __restrict__ dx, float* __restrict__ dp, int* __restrict__ status, int E, int64_t R,
-                     int64_t H, int KB, Coef c) {
+                     int64_t H, int KB, int csplit, Coef c) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = (uint8_t*)(((uintptr_t)smem_raw + 1023) & ~(uintptr_t)1023);
-    uint8_t* ring = smem;                                            // STAGES x (A | B)
-    Barriers* bars = (Barriers*)(smem + STAGES * STAGE_BYTES);
-    float* dp_part = (float*)(bars + 1);                             // [EPW][BM] per-warp-slot dp partials
-    int* tile_start = (int*)(dp_part + EPW * BM);                    // [E + 1]
-
+    const Smem sm = carve_smem(smem_raw);
+    Barriers* bars = sm.bars;
+    float* dp_part = (float*)sm.extra;                               // [EPW][BM] per-warp-slot dp partials
+    float* dp_cl = dp_part + EPW * BM;                               // [2][MAX_SPLIT][BM] cluster partials
+    uint64_t* dp_full = (uint64_t*)(dp_cl + 2 * MAX_SPLIT * BM);     // [2] leader: partials of all ranks in
+    uint64_t* dp_free = dp_full + 2;                                 // [2] other ranks: the leader read them
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int NT = (int)(H / BN);
+    const uint32_t crank = cluster_rank();
 
-    // tile prefix over experts (each CTA builds its own copy): counts in parallel, then one
-    // warp scans them (each lane a contiguous segment, shuffles across lanes)
-    for (int e = threadIdx.x; e < E; e += NUM_THREADS) {
-        const int64_t n = offsets[e + 1] - offsets[e];
-        tile_start[e + 1] = n > 0 ? (int)((n + BM - 1) / BM) : 0;
-    }
     if (threadIdx.x == 0) {
-        tile_start[0] = 0;
-        for (int s = 0; s < STAGES; ++s) {
-            mbar_init(&bars->full[s], 1);
-            mbar_init(&bars->empty[s], 1);
-        }
-        for (int a = 0; a < 2; ++a) {
-            mbar_init(&bars->tfull[a], 1);
-            mbar_init(&bars->tempty[a], NUM_EPI_THREADS);
-        }
-        mbar_init(&bars->mma_done, 1);
-        bars->abort = 0;
-        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    __syncthreads();
-    if (warp == 0) {
-        const int seg = (E + 31) / 32;
-        const int b = 1 + lane * seg, en = min(E + 1, b + seg);
-        int sum = 0;
-        for (int i = b; i < en; ++i) sum += tile_start[i];
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        int run = incl - sum;
-        for (int i = b; i < en; ++i) {
-            run += tile_start[i];
-            tile_start[i] = run;
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&dp_full[b], (uint32_t)((csplit - 1) * BM));
+            mbar_init(&dp_free[b], (uint32_t)BM);
         }
     }
-    if (warp == 1) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&bars->tmem_base)),
-                     "r"(TMEM_COLS)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = bars->tmem_base;
-    const int T = tile_start[E];
+    const Sched sc = make_sched(csplit);
+    uint32_t tmem;
+    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem);
+    const int* tile_start = sm.tile_start;
+    cluster_sync();                          // every CTA's barriers are initialised before any remote use
 
     if (warp == 0) {
-        // ------------------------------------------------ TMA producer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            uint32_t pending = 0;            // bit s: stage s has a load in flight of parity pend_par
-            uint32_t pend_par = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                int e;
-                int64_t row0, row_end;
-                tile_rows(tile_start, offsets, E, R, t, e, row0, row_end);
-                for (int nt = 0; ok && nt < NT; ++nt) {
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!mbar_wait(&bars->empty[stage], phase ^ 1, bars, status)) { ok = false; break; }
-                        mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
-                        uint8_t* sa = ring + stage * STAGE_BYTES;
-                        tma_load_2d(sa, &map_dy, kb * BK, (int)row0, &bars->full[stage]);
-                        tma_load_2d(sa + A_BYTES, &map_w, kb * BK, (int)((int64_t)e * H + (int64_t)nt * BN),
-                                    &bars->full[stage]);
-                        pending |= 1u << stage;
-                        pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
-                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                    }
-                }
-            }
-            // every load issued must land before the CTA exits: wait for each stage's last phase
-            for (int s2 = 0; s2 < STAGES; ++s2) {
-                if (!(pending & (1u << s2))) continue;
-                const uint32_t par = (pend_par >> s2) & 1u;
-                for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-                    if (mbar_try_wait(&bars->full[s2], par)) break;
-            }
-        }
+        // ------------------------------------------------ TMA producer: B = W_downᵀ rows e·H + nt·256 ..
+        if (lane == 0)
+            run_producer(sm, sc, &map_dy, offsets, E, R, T, NT, KB, status,
+                         [&](uint8_t* sb, int e, int nt, int kb, uint64_t* bar, uint64_t pol) {
+                             tma_load_2d_hint(sb, &map_w, kb * BK, (int)((int64_t)e * H + (int64_t)nt * BN), bar,
+                                              pol);
+                         });
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int job = 0;
-            bool ok = true;
-            for (int t = blockIdx.x; ok && t < T; t += gridDim.x) {
-                for (int nt = 0; ok && nt < NT; ++nt, ++job) {
-                    const int acc = job & 1;
-                    const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
-                    if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1, bars, status)) { ok = false; break; }
-                    tc_fence_after();
-                    const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
-                    for (int kb = 0; kb < KB; ++kb) {
-                        if (!mbar_wait(&bars->full[stage], phase, bars, status)) { ok = false; break; }
-                        tc_fence_after();
-                        const uint32_t sa = smem_addr(ring + stage * STAGE_BYTES);
-                        const uint64_t adesc = smem_desc(sa), bdesc = smem_desc(sa + A_BYTES);
-#pragma unroll
-                        for (int kk = 0; kk < BK / UK; ++kk) {
-                            // advance 16 bf16 (32 bytes = 2 descriptor units) along K inside the swizzled rows
-                            tc_mma(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2),
-                                   (kb > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc_commit(&bars->empty[stage]);          // ring stage free once these MMAs finish
-                        if (++stage == STAGES) { stage = 0; phase ^= 1; }
-                    }
-                    if (ok) tc_commit(&bars->tfull[acc]);        // accumulator complete
-                }
-            }
-            // all MMAs issued by this thread complete before TMEM is freed
-            tc_commit(&bars->mma_done);
-            for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-                if (mbar_try_wait(&bars->mma_done, 0)) break;
-        }
+        if (lane == 0) run_mma(sm, sc, tmem, T, NT, KB, status);
     } else {
         // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
         // A warp may read only the TMEM lanes of quadrant warp % 4; the EPW warps of a quadrant split
@@ -340,9 +99,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int slot = (warp - 2) >> 2;
         const int lrow = quad * 32 + lane;         // row within the tile
         const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
-        int job = 0;
+        int job = 0, it = 0;
         bool ok = true;
-        for (int t = blockIdx.x; t < T; t += gridDim.x) {
+        for (int t = sc.t0; t < T; t += sc.tstep, ++it) {
             int e;
             int64_t row0, row_end;
             tile_rows(tile_start, offsets, E, R, t, e, row0, row_end);
@@ -353,14 +112,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint16_t* dxr = dx + (valid ? row : 0) * 2 * H + slot * COLS_PER_WARP;
             float acc_dp = 0.0f;
             Vec<8> xb[2][2][XV];                   // [buffer][gate, linear][32-byte vector]
-            if (valid) {
+            if (valid) {                           // first chunk: (first N-tile of this CTA, 0)
+                const int64_t j1 = (int64_t)sc.n0 * BN;
 #pragma unroll
                 for (int v = 0; v < XV; ++v) {
-                    xb[0][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + 16 * v));
-                    xb[0][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + 16 * v));
+                    xb[0][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + j1 + 16 * v));
+                    xb[0][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + j1 + 16 * v));
                 }
             }
-            for (int nt = 0; nt < NT; ++nt, ++job) {
+            for (int nt = sc.n0; nt < NT; nt += sc.nstep, ++job) {
                 const int acc = job & 1;
                 const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
                 if (ok && !mbar_wait(&bars->tfull[acc], acc_phase, bars, status)) ok = false;
@@ -369,10 +129,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int k = 0; k < CPJ; ++k) {
                     const int cur = k & 1;
-                    // prefetch the next chunk of this row: (nt, k + 1), or (nt + 1, 0) after the last
+                    // prefetch the next chunk of this row: (nt, k + 1), or (next N-tile, 0) after the last
                     const bool last = (k + 1 == CPJ);
-                    if (valid && (!last || nt + 1 < NT)) {
-                        const int64_t jn = last ? (int64_t)(nt + 1) * BN : (int64_t)nt * BN + (k + 1) * CW;
+                    if (valid && (!last || nt + sc.nstep < NT)) {
+                        const int64_t jn = last ? (int64_t)(nt + sc.nstep) * BN : (int64_t)nt * BN + (k + 1) * CW;
 #pragma unroll
                         for (int v = 0; v < XV; ++v) {
                             xb[cur ^ 1][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + jn + 16 * v));
@@ -407,58 +167,36 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            // combine the EPW column slices of each row
+            // combine the EPW column slices of each row, then the csplit CTAs of the cluster: every
+            // rank pushes its partial into the leader's shared memory (double-buffered by M-tile
+            // parity) and the leader adds them in rank order, so dp does not depend on timing
             if (slot > 0) dp_part[slot * BM + lrow] = acc_dp;
-            epi_barrier();
-            if (slot == 0 && valid) {
+            epi_barrier(NUM_EPI_THREADS);
+            if (slot == 0) {
                 float s = acc_dp;
 #pragma unroll
                 for (int k = 1; k < EPW; ++k) s += dp_part[k * BM + lrow];
-                dp[row] = 16.0f * s;
+                if (csplit > 1) {
+                    const int b = it & 1;
+                    const uint32_t use_par = (uint32_t)((it >> 1) & 1);
+                    if (crank != 0) {
+                        if (it >= 2) mbar_wait_cluster(&dp_free[b], use_par ^ 1, bars, status);
+                        st_cluster_f32(cluster_addr(&dp_cl[(b * MAX_SPLIT + (int)crank) * BM + lrow], 0), s);
+                        mbar_arrive_cluster(cluster_addr(&dp_full[b], 0));
+                    } else {
+                        mbar_wait_cluster(&dp_full[b], use_par, bars, status);
+                        for (int k = 1; k < csplit; ++k) s += dp_cl[(b * MAX_SPLIT + k) * BM + lrow];
+                        for (int k = 1; k < csplit; ++k) mbar_arrive_cluster(cluster_addr(&dp_free[b], (uint32_t)k));
+                    }
+                }
+                if (crank == 0 && valid) dp[row] = 16.0f * s;
             }
-            epi_barrier();
+            epi_barrier(NUM_EPI_THREADS);
         }
     }
 
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    if (warp == 1) {
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
-    }
-}
-
-// ---------------------------------------------------------------- host side
-
-using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiled encode_fn() {
-    static EncodeTiled fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = (EncodeTiled)p;
-    });
-    return fn;
-}
-
-// 2-D bf16 tensor map: rows x cols (cols contiguous), box of box_rows x 64 columns, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
-    EncodeTiled fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {cols, rows};
-    const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+    cluster_sync();                          // no CTA leaves while another may still access its shared memory
+    pipeline_teardown(tmem);
 }
 
 }  // namespace
@@ -496,14 +234,11 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
     auto kernel = b4 ? dgrad_bwd_kernel<true> : dgrad_bwd_kernel<false>;
     cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e);
-    int dev = 0, sms = 0;
-    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
-    if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
-    // persistent: one CTA per SM, never more CTAs than M-tiles could need
-    const int64_t max_tiles = (R + BM - 1) / BM + E;
-    const int grid = (int)(max_tiles < sms ? max_tiles : sms);
-    kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_dy, map_w, (const uint16_t*)x, expert_offsets, p,
-                                                      (uint16_t*)dx, dp, status, (int)E, R, H, (int)(D / BK), c);
+    const int NT = (int)(H / BN);
+    const int csplit = NT < DGRAD_SPLIT ? NT : DGRAD_SPLIT;
+    e = launch_clusters(kernel, R, E, csplit, NUM_THREADS, SMEM_BYTES, stream, map_dy, map_w, (const uint16_t*)x,
+                        expert_offsets, p, (uint16_t*)dx, dp, status, (int)E, R, H, (int)(D / BK), csplit, c);
+    if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return SITU_GLU_OK;

@@ -1,0 +1,183 @@
+// situ_glu_gateup.cu — gate/up projection grouped GEMM on the 5th-generation tensor cores
+// (tcgen05, TMA, TMEM), with the SiTU-GLU forward fused into its epilogue.
+//
+// "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出": a routed
+// row of expert e computes a_e = SiTU(W_gate,e·h, W_up,e·h) from its dispatched input h.
+// "Frontier-scale RL with Kimi K3", section "Streaming activations": the backward keeps only the
+// bf16 pre-activation x = [W_gate,e·h | W_up,e·h]; the forward reads x and writes a in bf16.
+// This kernel computes both projections of a row on the tensor cores and, from the fp32
+// accumulators, writes the bf16 x that the backward will read and out = a computed from that
+// same bf16 x, so the result equals the unfused projection followed by situ_glu_fwd, with one
+// fewer round trip of x through memory.
+//
+// The GEMM pipeline is the one in situ_tc.cuh with A = h and a B tile made of two 128-row
+// halves: rows nt·128 .. of W_gate,e and the same rows of W_up,e, so accumulator column c < 128
+// holds gate column nt·128 + c and column 128 + c the matching linear column. Epilogue: EPW warps
+// per 32-lane TMEM quadrant, each owning 128/EPW of a job's 128 column pairs; a thread owns one
+// row, reads 32 gate and 32 linear accumulators per chunk, rounds them to bf16 (nearest even),
+// evaluates the forward on the rounded values and writes x (both halves) and out with 32-byte
+// stores.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "../../include/situ_glu.h"
+#include "situ_device.cuh"
+#include "situ_host.h"
+#include "situ_math.cuh"
+#include "situ_tc.cuh"
+
+namespace {
+
+using namespace situ;
+using namespace situ_host;
+using namespace situ_tc;
+
+constexpr int HN = BN / 2;                   // column pairs per job (128 gate + 128 linear columns)
+constexpr int EPW = 2;                       // epilogue warps per 32-lane TMEM quadrant
+constexpr int CW = 32;                       // column pairs per chunk
+constexpr int NUM_EPI_THREADS = 4 * EPW * 32;
+constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;  // warp 0 TMA, warp 1 MMA, then the epilogue
+constexpr int PAIRS_PER_WARP = HN / EPW;
+constexpr int CPJ = PAIRS_PER_WARP / CW;     // chunks per job per epilogue warp
+static_assert(CPJ >= 1 && PAIRS_PER_WARP % CW == 0, "whole chunks per warp");
+constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 16;
+constexpr int CSPLIT = 8;                    // CTAs sharing an M-tile (each every 8th N-tile)
+
+template <bool BETA4>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gateup_fwd_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                      const int64_t* __restrict__ offsets, uint16_t* __restrict__ x, uint16_t* __restrict__ out,
+                      int* __restrict__ status, int E, int64_t R, int64_t H, int KB, int csplit, Coef c) {
+    extern __shared__ uint8_t smem_raw[];
+    const Smem sm = carve_smem(smem_raw);
+    Barriers* bars = sm.bars;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int NT = (int)(H / HN);
+
+    const Sched sc = make_sched(csplit);
+    uint32_t tmem;
+    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer: B = W_gate,e and W_up,e rows nt·128 ..
+        if (lane == 0)
+            run_producer(sm, sc, &map_h, offsets, E, R, T, NT, KB, status,
+                         [&](uint8_t* sb, int e, int nt, int kb, uint64_t* bar, uint64_t pol) {
+                             const int64_t r0 = (int64_t)e * 2 * H + (int64_t)nt * HN;
+                             tma_load_2d_hint(sb, &map_w, kb * BK, (int)r0, bar, pol);
+                             tma_load_2d_hint(sb + HN * BK * 2, &map_w, kb * BK, (int)(r0 + H), bar, pol);
+                         });
+    } else if (warp == 1) {
+        // ------------------------------------------------ MMA issuer
+        if (lane == 0) run_mma(sm, sc, tmem, T, NT, KB, status);
+    } else {
+        // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
+        const int quad = warp & 3;
+        const int slot = (warp - 2) >> 2;
+        const int lrow = quad * 32 + lane;
+        const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+        int job = 0;
+        bool ok = true;
+        for (int t = sc.t0; t < T; t += sc.tstep) {
+            int e;
+            int64_t row0, row_end;
+            tile_rows(sm.tile_start, offsets, E, R, t, e, row0, row_end);
+            const int64_t row = row0 + lrow;
+            const bool valid = ok && row >= 0 && row < row_end;
+            uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * PAIRS_PER_WARP;
+            uint16_t* outr = out + (valid ? row : 0) * H + slot * PAIRS_PER_WARP;
+            for (int nt = sc.n0; nt < NT; nt += sc.nstep, ++job) {
+                const int acc = job & 1;
+                const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
+                if (ok && !mbar_wait(&bars->tfull[acc], acc_phase, bars, status)) ok = false;
+                ok = __all_sync(0xffffffffu, ok);                 // tcgen05.ld below is warp-collective
+                tc_fence_after();
+#pragma unroll
+                for (int k = 0; k < CPJ; ++k) {
+                    uint32_t gr[CW], lr[CW];
+                    if (ok) {
+                        const uint32_t col = (uint32_t)(acc * BN + slot * PAIRS_PER_WARP + k * CW);
+                        tc_ld_issue<CW>(tmem + t_lane + col, gr);
+                        tc_ld_issue<CW>(tmem + t_lane + col + HN, lr);
+                        tc_wait_ld();
+                    }
+                    if (k + 1 == CPJ) {
+                        tc_fence_before();
+                        mbar_arrive(&bars->tempty[acc]);       // accumulator may be overwritten
+                    }
+                    if (ok && valid) {
+                        const int64_t j0 = (int64_t)nt * HN + k * CW;
+#pragma unroll
+                        for (int v = 0; v < CW / 16; ++v) {
+                            Vec<8> xg, xl, o;
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                const int q = 16 * v + 2 * i;
+                                xg.w[i] = pack_bf16x2(__uint_as_float(gr[q]), __uint_as_float(gr[q + 1]));
+                                xl.w[i] = pack_bf16x2(__uint_as_float(lr[q]), __uint_as_float(lr[q + 1]));
+                                const float a0 = situ::fwd<BETA4>(bf16_lo(xg.w[i]), bf16_lo(xl.w[i]), c);
+                                const float a1 = situ::fwd<BETA4>(bf16_hi(xg.w[i]), bf16_hi(xl.w[i]), c);
+                                o.w[i] = pack_bf16x2(a0, a1);
+                            }
+                            st_stream<8>((Vec<8>*)(xr + j0 + 16 * v), xg);
+                            st_stream<8>((Vec<8>*)(xr + H + j0 + 16 * v), xl);
+                            st_stream<8>((Vec<8>*)(outr + j0 + 16 * v), o);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    pipeline_teardown(tmem);
+}
+
+}  // namespace
+
+extern "C" {
+
+int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* expert_offsets, int64_t E, void* x,
+                        void* out, int* status, int64_t R, int64_t H, int64_t D, float beta, float lbeta,
+                        cudaStream_t stream) {
+    int st = check_shape(R, H, beta, lbeta);
+    if (st != SITU_GLU_OK) return st;
+    if (D <= 0 || D % BK != 0 || H % HN != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
+    if (R > INT32_MAX || E * 2 * H > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
+    if (R == 0) return SITU_GLU_OK;
+    if (!h || !w_gate_up || !expert_offsets || !x || !out) return SITU_GLU_INVALID_ARG;
+    if (!aligned(h, 16) || !aligned(w_gate_up, 16) || !aligned(x, 32) || !aligned(out, 32) ||
+        !aligned(expert_offsets, 8) || (status && !aligned(status, 4)))
+        return SITU_GLU_INVALID_ARG;
+    const Range rh = range_of(h, R * D * 2), rw = range_of(w_gate_up, E * 2 * H * D * 2);
+    const Range ro = range_of(expert_offsets, (E + 1) * 8);
+    const Range rx = range_of(x, R * 2 * H * 2), rout = range_of(out, R * H * 2);
+    for (Range in : {rh, rw, ro}) {
+        if (overlap(rx, in) || overlap(rout, in)) return SITU_GLU_OVERLAP;
+        if (status && overlap(range_of(status, 4), in)) return SITU_GLU_OVERLAP;
+    }
+    if (overlap(rx, rout)) return SITU_GLU_OVERLAP;
+    if (status && (overlap(range_of(status, 4), rx) || overlap(range_of(status, 4), rout))) return SITU_GLU_OVERLAP;
+
+    CUtensorMap map_h, map_w;
+    if (!make_map(&map_h, h, (uint64_t)R, (uint64_t)D, BM)) return cuda_fail(cudaErrorInvalidValue);
+    if (!make_map(&map_w, w_gate_up, (uint64_t)(E * 2 * H), (uint64_t)D, HN)) return cuda_fail(cudaErrorInvalidValue);
+
+    const Coef c = make_coef(beta, lbeta);
+    const bool b4 = fast_path(beta, lbeta);
+    auto kernel = b4 ? gateup_fwd_kernel<true> : gateup_fwd_kernel<false>;
+    cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_fail(e);
+    const int NT = (int)(H / HN);
+    const int csplit = NT < CSPLIT ? NT : CSPLIT;
+    int grid = 0;
+    if ((e = (cudaError_t)persistent_grid(R, E, csplit, &grid)) != cudaSuccess) return cuda_fail(e);
+    kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_h, map_w, expert_offsets, (uint16_t*)x, (uint16_t*)out,
+                                                      status, (int)E, R, H, (int)(D / BK), csplit, c);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e);
+    return SITU_GLU_OK;
+}
+
+}  // extern "C"

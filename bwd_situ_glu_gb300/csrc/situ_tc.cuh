@@ -1,0 +1,530 @@
+// situ_tc.cuh — the expert-grouped GEMM pipeline on the 5th-generation tensor cores (tcgen05,
+// TMA, TMEM, mbarriers) shared by the two fused kernels: the down-projection dgrad with the
+// SiTU-GLU backward in its epilogue, and the gate/up projection with the SiTU-GLU forward in its
+// epilogue. Each kernel supplies only its B-tile loads and its epilogue.
+//
+// Problem: rows are grouped by expert (expert e owns rows offsets[e] .. offsets[e+1]-1); for every
+// row r of expert e and output column n, C[r, n] = Σ_k A[r, k]·B_e[n, k] with A and B_e bf16 and
+// K-major (k contiguous), C accumulated in fp32.
+//
+// Work decomposition: an M-tile is 128 consecutive rows of ONE expert (an expert with n rows has
+// ceil(n/128) M-tiles; the last one is partial and the epilogue skips the rows past the expert's
+// end). A job is one M-tile times one 256-column N-tile. CTAs are persistent (one per SM); a
+// group of CSPLIT consecutive CTAs takes M-tiles g, g + groups, ... and its k-th CTA the N-tiles
+// k, k + CSPLIT, ... of each (see Sched).
+//
+// Per-CTA roles:
+//   warp 0, one thread   TMA producer: per 64-wide K-block, A [128 x 64] and B [256 x 64] (bf16,
+//                        128-byte swizzle) into a STAGES-deep shared-memory ring, completion
+//                        signalled on the stage's "full" mbarrier (transaction bytes);
+//   warp 1               allocates 512 TMEM columns (two 128 x 256 fp32 accumulators); one thread
+//                        issues tcgen05.mma (M = 128, N = 256, K = 16) and commits to mbarriers
+//                        that free ring stages ("empty") and hand accumulators to the epilogue
+//                        ("tfull"); the epilogue hands them back through "tempty";
+//   warps 2 ..           the kernel's epilogue.
+// Every wait is bounded (WAIT_LIMIT polls): on a timeout the CTA sets its abort flag and the
+// caller's status word, stops issuing work, waits (bounded) for what it already issued, frees
+// its TMEM and returns.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <mutex>
+
+namespace situ_tc {
+
+constexpr int BM = 128;                      // rows per M-tile (TMEM lanes)
+constexpr int BN = 256;                      // accumulator columns per job
+constexpr int BK = 64;                       // K per ring stage (128 bytes of bf16: one swizzle row)
+constexpr int UK = 16;                       // K per tcgen05.mma (kind::f16)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK * 2;         // 16 KB
+constexpr int B_BYTES = BN * BK * 2;         // 32 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 columns
+constexpr int MAX_EXPERTS = 4096;
+constexpr uint32_t WAIT_LIMIT = 1u << 22;    // polls of a try_wait before giving up (~1-2 s)
+
+struct alignas(8) Barriers {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tfull[2];
+    uint64_t tempty[2];
+    uint64_t mma_done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+// Dynamic shared memory: [pad to 1024] ring | Barriers | tile_start[MAX_EXPERTS + 1] | extra.
+constexpr int SMEM_FIXED_BYTES = 1024 + STAGES * STAGE_BYTES + (int)sizeof(Barriers) + (MAX_EXPERTS + 1) * 4;
+
+struct Smem {
+    uint8_t* ring;
+    Barriers* bars;
+    int* tile_start;
+    uint8_t* extra;     // 16-byte aligned kernel-specific area
+};
+
+__device__ __forceinline__ Smem carve_smem(uint8_t* raw) {
+    Smem s;
+    s.ring = (uint8_t*)(((uintptr_t)raw + 1023) & ~(uintptr_t)1023);
+    s.bars = (Barriers*)(s.ring + STAGES * STAGE_BYTES);
+    s.tile_start = (int*)(s.bars + 1);
+    s.extra = (uint8_t*)(((uintptr_t)(s.tile_start + MAX_EXPERTS + 1) + 15) & ~(uintptr_t)15);
+    return s;
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(b)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(b)), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(b)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}"
+        : "=r"(ok)
+        : "r"(smem_addr(b)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Bounded wait; on a timeout sets the CTA's abort flag and the caller's status word.
+__device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Barriers* bars, int* status) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(b, parity)) return true;
+        if (i > 64 && *(volatile int*)&bars->abort) return false;
+    }
+    *(volatile int*)&bars->abort = 1;
+    if (status) atomicExch(status, 1);
+    return false;
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+            smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// The same with an L2 eviction-priority policy (from make_policy) for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, int c0, int c1, uint64_t* bar,
+                                                 uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+enum class L2Hint { normal, first, last };
+
+template <L2Hint P>
+__device__ __forceinline__ uint64_t make_policy() {
+    uint64_t pol;
+    if constexpr (P == L2Hint::last)
+        asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
+    else if constexpr (P == L2Hint::first)
+        asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
+    else
+        asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
+    return pol;
+}
+
+// L2 priorities of the two operands: the A tile (activations, re-read once per N-tile) and the
+// B tiles (weights, read by the few M-tiles of their expert at nearly the same time).
+constexpr L2Hint kHintA = L2Hint::normal;
+constexpr L2Hint kHintB = L2Hint::normal;
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// Shared-memory matrix descriptor of a K-major bf16 tile with 128-byte swizzle: rows of 128 bytes,
+// 8-row groups 1024 bytes apart (stride byte offset), version bits 46-47 = 1, swizzle mode 2.
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);          // start address
+    d |= (uint64_t)1 << 16;                           // leading byte offset (unused for swizzled K-major)
+    d |= (uint64_t)(1024 >> 4) << 32;                 // stride byte offset: 8 rows x 128 B
+    d |= (uint64_t)1 << 46;                           // descriptor version
+    d |= (uint64_t)2 << 61;                           // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor, kind::f16: fp32 accumulate, bf16 A and B, both K-major, N = 256, M = 128.
+constexpr uint32_t IDESC = (1u << 4)           // D format fp32
+                         | (1u << 7)           // A format bf16
+                         | (1u << 10)          // B format bf16
+                         | ((uint32_t)(BN >> 3) << 17)
+                         | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
+            d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_commit(uint64_t* bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Issue a load of N consecutive fp32 columns (N = 16 or 32) of this thread's TMEM lane; the
+// registers are valid after tc_wait_ld().
+template <int N>
+__device__ __forceinline__ void tc_ld_issue(uint32_t taddr, uint32_t (&r)[N]) {
+    if constexpr (N == 32) {
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,"
+            "%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+              "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]),
+              "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]),
+              "=r"(r[30]), "=r"(r[31])
+            : "r"(taddr));
+    } else {
+        static_assert(N == 16, "16 or 32 columns");
+        asm volatile(
+            "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+            : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+              "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+            : "r"(taddr));
+    }
+}
+
+__device__ __forceinline__ void tc_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// N consecutive fp32 columns of this thread's TMEM lane, waited for.
+template <int N>
+__device__ __forceinline__ void tc_ld(uint32_t taddr, float (&v)[N]) {
+    uint32_t r[N];
+    tc_ld_issue<N>(taddr, r);
+    tc_wait_ld();
+#pragma unroll
+    for (int i = 0; i < N; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// ---------------------------------------------------------------- thread-block clusters
+
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of all CTAs of the cluster; orders shared-memory accesses across the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release;\n barrier.cluster.wait.acquire;" ::: "memory");
+}
+
+// The shared::cluster address of this CTA's shared variable p in the CTA of cluster rank `rank`.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_addr(p)), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ void st_cluster_f32(uint32_t caddr, float v) {
+    asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(caddr), "f"(v) : "memory");
+}
+
+// Arrive (release at cluster scope) on an mbarrier of any CTA of the cluster.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+// Bounded wait with acquire at cluster scope (data written by other CTAs of the cluster before
+// their arrive is visible afterwards); on a timeout sets the abort flag and the status word.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, Barriers* bars, int* status) {
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        uint32_t ok;
+        asm volatile(
+            "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+            " selp.u32 %0, 1, 0, p;\n}"
+            : "=r"(ok)
+            : "r"(smem_addr(b)), "r"(parity)
+            : "memory");
+        if (ok) return true;
+        if (i > 64 && *(volatile int*)&bars->abort) return false;
+    }
+    *(volatile int*)&bars->abort = 1;
+    if (status) atomicExch(status, 1);
+    return false;
+}
+
+// Named barrier over the epilogue warps only (id 1; id 0 is __syncthreads).
+__device__ __forceinline__ void epi_barrier(int nthreads) { asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory"); }
+
+// M-tile t -> (expert, first row, end row of the expert).
+__device__ __forceinline__ void tile_rows(const int* tile_start, const int64_t* off, int E, int64_t R, int t,
+                                          int& e, int64_t& row0, int64_t& row_end) {
+    int lo = 0, hi = E - 1;                 // last e with tile_start[e] <= t
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    row0 = off[e] + (int64_t)(t - tile_start[e]) * BM;
+    row_end = off[e + 1] < R ? off[e + 1] : R;     // clamped: malformed offsets never index past R
+}
+
+// ---------------------------------------------------------------- work assignment
+
+// CSPLIT consecutive CTAs share each M-tile, CTA rank k taking N-tiles k, k + CSPLIT, ...: at any
+// moment only gridDim.x / CSPLIT distinct A tiles (128 rows x K) are being streamed, so each one
+// stays in L2 across the N-tiles that re-read it. gridDim.x is a multiple of CSPLIT.
+struct Sched {
+    int t0, tstep;      // M-tiles t0, t0 + tstep, ...
+    int n0, nstep;      // N-tiles n0, n0 + nstep, ... of each M-tile
+};
+
+__device__ __forceinline__ Sched make_sched(int csplit) {
+    Sched s;
+    s.t0 = (int)blockIdx.x / csplit;
+    s.tstep = (int)gridDim.x / csplit;
+    s.n0 = (int)blockIdx.x % csplit;
+    s.nstep = csplit;
+    return s;
+}
+
+// ---------------------------------------------------------------- pipeline phases
+
+// All threads: per-expert M-tile prefix (each CTA builds its own copy: counts in parallel, then
+// one warp scans them, each lane a contiguous segment, shuffles across lanes), barrier init, TMEM
+// allocation by warp 1. Returns the number of M-tiles; *tmem receives the TMEM base address.
+__device__ __forceinline__ int pipeline_setup(const Smem& sm, const int64_t* offsets, int E, int num_epi_threads,
+                                              uint32_t* tmem) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    Barriers* bars = sm.bars;
+    int* tile_start = sm.tile_start;
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+        const int64_t n = offsets[e + 1] - offsets[e];
+        tile_start[e + 1] = n > 0 ? (int)((n + BM - 1) / BM) : 0;
+    }
+    if (threadIdx.x == 0) {
+        tile_start[0] = 0;
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->tfull[a], 1);
+            mbar_init(&bars->tempty[a], (uint32_t)num_epi_threads);
+        }
+        mbar_init(&bars->mma_done, 1);
+        bars->abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int seg = (E + 31) / 32;
+        const int b = 1 + lane * seg, en = min(E + 1, b + seg);
+        int sum = 0;
+        for (int i = b; i < en; ++i) sum += tile_start[i];
+        int incl = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - sum;
+        for (int i = b; i < en; ++i) {
+            run += tile_start[i];
+            tile_start[i] = run;
+        }
+    }
+    if (warp == 1) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_addr(&bars->tmem_base)),
+                     "r"(TMEM_COLS)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    *tmem = bars->tmem_base;
+    return tile_start[E];
+}
+
+// One thread of warp 0. load_b(b_smem, e, nt, kb, bar, policy) issues the B-tile TMA loads
+// (B_BYTES in total) of expert e, N-tile nt, K-block kb; A comes from map_a at (kb·BK, row0).
+template <class LoadB>
+__device__ __forceinline__ void run_producer(const Smem& sm, const Sched& sc, const CUtensorMap* map_a,
+                                             const int64_t* offsets, int E, int64_t R, int T, int NT, int KB,
+                                             int* status, LoadB load_b) {
+    Barriers* bars = sm.bars;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pending = 0;            // bit s: stage s has a load in flight of parity pend_par
+    uint32_t pend_par = 0;
+    const uint64_t pol_a = make_policy<kHintA>(), pol_b = make_policy<kHintB>();
+    bool ok = true;
+    for (int t = sc.t0; ok && t < T; t += sc.tstep) {
+        int e;
+        int64_t row0, row_end;
+        tile_rows(sm.tile_start, offsets, E, R, t, e, row0, row_end);
+        for (int nt = sc.n0; ok && nt < NT; nt += sc.nstep) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1, bars, status)) { ok = false; break; }
+                mbar_expect_tx(&bars->full[stage], STAGE_BYTES);
+                uint8_t* sa = sm.ring + stage * STAGE_BYTES;
+                tma_load_2d_hint(sa, map_a, kb * BK, (int)row0, &bars->full[stage], pol_a);
+                load_b(sa + A_BYTES, e, nt, kb, &bars->full[stage], pol_b);
+                pending |= 1u << stage;
+                pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+        }
+    }
+    // every load issued must land before the CTA exits: wait for each stage's last phase
+    for (int s2 = 0; s2 < STAGES; ++s2) {
+        if (!(pending & (1u << s2))) continue;
+        const uint32_t par = (pend_par >> s2) & 1u;
+        for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
+            if (mbar_try_wait(&bars->full[s2], par)) break;
+    }
+}
+
+// One thread of warp 1: the MMA issuer.
+__device__ __forceinline__ void run_mma(const Smem& sm, const Sched& sc, uint32_t tmem, int T, int NT, int KB,
+                                        int* status) {
+    Barriers* bars = sm.bars;
+    int stage = 0;
+    uint32_t phase = 0;
+    int job = 0;
+    bool ok = true;
+    for (int t = sc.t0; ok && t < T; t += sc.tstep) {
+        for (int nt = sc.n0; ok && nt < NT; nt += sc.nstep, ++job) {
+            const int acc = job & 1;
+            const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
+            if (!mbar_wait(&bars->tempty[acc], acc_phase ^ 1, bars, status)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t d_tmem = tmem + (uint32_t)(acc * BN);
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait(&bars->full[stage], phase, bars, status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_addr(sm.ring + stage * STAGE_BYTES);
+                const uint64_t adesc = smem_desc(sa), bdesc = smem_desc(sa + A_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk) {
+                    // advance 16 bf16 (32 bytes = 2 descriptor units) along K inside the swizzled rows
+                    tc_mma(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), (kb > 0 || kk > 0) ? 1u : 0u);
+                }
+                tc_commit(&bars->empty[stage]);          // ring stage free once these MMAs finish
+                if (++stage == STAGES) { stage = 0; phase ^= 1; }
+            }
+            if (ok) tc_commit(&bars->tfull[acc]);        // accumulator complete
+        }
+    }
+    // all MMAs issued by this thread complete before TMEM is freed
+    tc_commit(&bars->mma_done);
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
+        if (mbar_try_wait(&bars->mma_done, 0)) break;
+}
+
+// All threads, at the end: TMEM is freed by warp 1 once every role has finished with it.
+__device__ __forceinline__ void pipeline_teardown(uint32_t tmem) {
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if ((threadIdx.x >> 5) == 1) {
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(TMEM_COLS) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiled = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                 const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                 CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiled encode_fn() {
+    static EncodeTiled fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = (EncodeTiled)p;
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor map: rows x cols (cols contiguous), box of box_rows x 64 columns, 128-byte swizzle.
+// Rows past the end read as zero.
+inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * 2};
+    const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Launch of a persistent kernel as clusters of csplit CTAs (csplit = 1: plain CTAs): as many
+// clusters as can be resident at once, never more than there are M-tiles.
+template <class... KArgs, class... Args>
+inline cudaError_t launch_clusters(void (*kernel)(KArgs...), int64_t R, int64_t E, int csplit, int threads,
+                                   int smem, cudaStream_t stream, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)csplit;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3((unsigned)threads);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3((unsigned)(sms / csplit * csplit));
+    int clusters = 0;
+    e = cudaOccupancyMaxActiveClusters(&clusters, (const void*)kernel, &cfg);
+    if (e != cudaSuccess) return e;
+    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    const int64_t tiles = (R + BM - 1) / BM + E;
+    if (clusters > tiles) clusters = (int)tiles;
+    cfg.gridDim = dim3((unsigned)(clusters * csplit));
+    return cudaLaunchKernelEx(&cfg, kernel, args...);
+}
+
+// Persistent grid: one CTA per SM, a multiple of csplit, never more CTAs than the jobs could need.
+inline int persistent_grid(int64_t R, int64_t E, int csplit, int* grid) {
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return (int)e;
+    const int64_t max_ctas = ((R + BM - 1) / BM + E) * csplit;
+    int64_t g = max_ctas < sms ? max_ctas : sms;
+    g = g / csplit * csplit;
+    *grid = (int)(g > 0 ? g : csplit);
+    return 0;
+}
+
+}  // namespace situ_tc

@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 1
+#define SITU_GLU_VERSION_MINOR 2
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -189,6 +189,37 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
                               const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
                               float* dp, int* status, int64_t R, int64_t H, int64_t D, float beta,
                               float lbeta, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Gate/up projection fused with the forward (tensor cores).
+ *
+ * "Kimi K3 模型结构（9）：显存", section "MoE 反向：推一下为什么可以不存 expert 输出": a routed row
+ * of expert e computes a_e = SiTU(W_gate,e·h, W_up,e·h) from its dispatched input h.
+ * "Frontier-scale RL with Kimi K3", section "Streaming activations": only the bf16 pre-activation
+ * x = [W_gate,e·h | W_up,e·h] is kept for the backward. This entry point computes both
+ * projections of every routed row on the tensor cores (tcgen05, fp32 accumulation in tensor
+ * memory) and, in the same kernel, writes x rounded to bf16 (nearest even) and
+ * out = G(gate)·L(linear) evaluated on that bf16 x: the same values as the projection followed
+ * by situ_glu_fwd, without reading x back.
+ *
+ *   h          device, bf16 [R,D], read only: each routed row's dispatched input, rows grouped
+ *              by expert
+ *   w_gate_up  device, bf16 [E,2H,D], read only, K-major: rows 0..H-1 of expert e are W_gate,e
+ *              (row j = the weights of gate column j), rows H..2H-1 are W_up,e, so
+ *              x[r,n] = Σ_d h[r,d]·w_gate_up[e,n,d]
+ *   expert_offsets device, int64 [E+1]: as for situ_glu_bwd_router_dgrad
+ *   x          device, bf16 [R,2H], written: the saved pre-activation (gate half, linear half)
+ *   out        device, bf16 [R,H], written: SiTU-GLU of x
+ *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
+ *              the kernel exceeded its limit (then x and out are incomplete). Zero it beforehand.
+ *   R, H, D, E sizes: H % 128 == 0, D % 64 == 0, 1 <= E <= 4096, R < 2^31, E*2H < 2^31
+ *   Pointers to h and w_gate_up must be 16-byte aligned (TMA), to x and out 32-byte aligned.
+ * x and out may not overlap each other or any input (SITU_GLU_OVERLAP). Returns
+ * SITU_GLU_INVALID_ARG for shapes or alignments outside these limits.
+ * --------------------------------------------------------------------------------------- */
+int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* expert_offsets,
+                        int64_t E, void* x, void* out, int* status, int64_t R, int64_t H,
+                        int64_t D, float beta, float lbeta, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code (unknown codes included). */
 const char* situ_glu_status_string(int status);

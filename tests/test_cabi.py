@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10100
+    assert sg.version() == 10200
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
@@ -162,3 +162,73 @@ def test_fp8_entry_points_validate_before_any_launch(lib):
     assert bwd8(lib, xq, xs, g, p, xq, dp, R, H) == OVERLAP      # dx over the codes
     assert bwd8(lib, xq, xs, g, p, dx, xs, R, H) == OVERLAP      # dp over the scales
     assert bwd8(lib, xq, xs, g, p, dx, dx + 8, R, H) == OVERLAP  # dp inside dx
+
+
+# ---------------------------------------------------------------- tensor-core entry points
+
+def dgrad(lib, x, dy, wt, off, E, p, dx, dp, st, R, H, D, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_bwd_router_dgrad(x, dy, wt, off, E, p, dx, dp, st, R, H, D, beta, lbeta, None)
+
+
+def gateup(lib, h, w, off, E, x, out, st, R, H, D, beta=4.0, lbeta=25.0):
+    return lib.situ_glu_fwd_gateup(h, w, off, E, x, out, st, R, H, D, beta, lbeta, None)
+
+
+def test_dgrad_validates_before_any_launch(lib):
+    R, H, D, E = 4, 256, 64, 2       # x, dx 4 KB; dy 512 B; wt 64 KB
+    x, dy, wt, off, p = A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20)
+    dx, dp, st = B, B + (1 << 20), B + (2 << 20)
+    args = [x, dy, wt, off, E, p, dx, dp, st]
+    assert dgrad(lib, *[None] * 4, E, None, None, None, None, 0, H, D) == OK
+    assert dgrad(lib, *args, R, 128, D) == INVALID                 # H % 256
+    assert dgrad(lib, *args, R, H, 96) == INVALID                  # D % 64
+    assert dgrad(lib, *args, R, H, 0) == INVALID
+    assert dgrad(lib, *args, -1, H, D) == INVALID
+    assert dgrad(lib, *args, R, H, D, 0.0) == INVALID
+    for bad_e in (0, 4097):
+        a = list(args)
+        a[4] = bad_e
+        assert dgrad(lib, *a, R, H, D) == INVALID
+    for i in (0, 1, 2, 3, 5, 6, 7):                                # every pointer but status is required
+        a = list(args)
+        a[i] = None
+        assert dgrad(lib, *a, R, H, D) == INVALID
+    for i, misalign in ((0, 16), (6, 16), (1, 8), (2, 8), (3, 4), (5, 2), (7, 2), (8, 2)):
+        a = list(args)
+        a[i] += misalign                                            # x, dx need 32 B; dy, wt 16 B; ...
+        assert dgrad(lib, *a, R, H, D) == INVALID, i
+    assert dgrad(lib, x, dy, wt, off, E, p, x + 1024, dp, st, R, H, D) == OVERLAP      # dx over x
+    assert dgrad(lib, x, dy, wt, off, E, p, dx, wt + 64, st, R, H, D) == OVERLAP      # dp over wt
+    assert dgrad(lib, x, dy, wt, off, E, p, dx, dx + 512, st, R, H, D) == OVERLAP     # dp inside dx
+    assert dgrad(lib, x, dy, wt, off, E, p, dx, dp, off, R, H, D) == OVERLAP          # status over offsets
+    assert dgrad(lib, x, dy, wt, off, E, p, dx, dp, dx + 4, R, H, D) == OVERLAP       # status inside dx
+
+
+def test_gateup_validates_before_any_launch(lib):
+    R, H, D, E = 4, 128, 64, 2       # h 512 B; w 64 KB; x 2 KB; out 1 KB
+    h, w, off = A, A + (1 << 20), A + (2 << 20)
+    x, out, st = B, B + (1 << 20), B + (2 << 20)
+    args = [h, w, off, E, x, out, st]
+    assert gateup(lib, None, None, None, E, None, None, None, 0, H, D) == OK
+    assert gateup(lib, *args, R, 64, D) == INVALID                 # H % 128
+    assert gateup(lib, *args, R, 192, D) == INVALID
+    assert gateup(lib, *args, R, H, 32) == INVALID                 # D % 64
+    assert gateup(lib, *args, -1, H, D) == INVALID
+    assert gateup(lib, *args, R, H, D, 4.0, float("nan")) == INVALID
+    for bad_e in (0, -1, 4097):
+        a = list(args)
+        a[3] = bad_e
+        assert gateup(lib, *a, R, H, D) == INVALID
+    for i in (0, 1, 2, 4, 5):                                      # every pointer but status is required
+        a = list(args)
+        a[i] = None
+        assert gateup(lib, *a, R, H, D) == INVALID
+    for i, misalign in ((0, 8), (1, 8), (2, 4), (4, 16), (5, 16), (6, 2)):
+        a = list(args)
+        a[i] += misalign                                            # h, w need 16 B; x, out 32 B; ...
+        assert gateup(lib, *a, R, H, D) == INVALID, i
+    assert gateup(lib, h, w, off, E, h + 256, out, st, R, H, D) == OVERLAP      # x over h
+    assert gateup(lib, h, w, off, E, x, w + 1024, st, R, H, D) == OVERLAP      # out over w
+    assert gateup(lib, h, w, off, E, x, x + 1024, st, R, H, D) == OVERLAP      # out inside x
+    assert gateup(lib, h, w, off, E, x, off - 32, st, R, H, D) == OVERLAP      # out over offsets
+    assert gateup(lib, h, w, off, E, x, out, out + 8, R, H, D) == OVERLAP      # status inside out

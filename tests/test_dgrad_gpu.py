@@ -45,6 +45,9 @@ CASES = {
     "partial_tiles": ([100, 60], 256, 128),
     "empty_experts": ([0, 300, 1, 129, 0, 77, 0], 512, 256),
     "real_widths": ([200, 0, 317, 128, 90, 250, 33, 400, 1, 255, 256, 129], 3072, 3584),
+    # H / 256 N-tiles shared by a cluster of min(4, H / 256) CTAs: 3 of 3, and 5 over 4 (uneven)
+    "three_way_split": ([129, 0, 200], 768, 64),
+    "uneven_split": ([300, 77], 1280, 128),
 }
 
 

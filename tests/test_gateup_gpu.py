@@ -1,0 +1,165 @@
+"""Parity of the fused gate/up projection (tcgen05 grouped GEMM + SiTU-GLU forward) with the
+oracle: x = [W_gate,e·h | W_up,e·h] in fp64 (numpy matmul), rounded to bf16 by the oracle's
+round-to-nearest-even, and out = G·L in fp64 on those bf16 values.
+
+x is a rounded fp32 accumulation. An fp32 sum of D products differs from the exact sum by a
+small multiple of 2^-24·Σ_d|h_d·w_d|, so where the exact value lies that close to a midpoint
+between two bf16 values either neighbour is a correct rounding. The test therefore requires
+x_gpu = RNE(x_exact + δ) for some |δ| <= 2^-20·Σ_d|h_d·w_d| (rounding is monotone, so that is
+every bf16 value in the closed range [RNE(x_exact - ε), RNE(x_exact + ε)], several values wide
+where |x| is small next to Σ|h·w|; the margin is 16x the random-walk size of an fp32 sum of 3584
+terms) and counts how often it differs from RNE(x_exact). Several results being correct there,
+out is compared, with the bf16 tolerance, to the oracle's forward at the admissible x the
+kernel chose."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import situ_inputs as si
+from _parity import Parity, bf16_bits_to_f64, bits_of, sample_rows
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+ACC_EPS = 2.0 ** -20
+
+
+@pytest.fixture(scope="module")
+def sg(cuda_lib):
+    assert torch.cuda.is_available()
+    return cuda_lib
+
+
+def make(counts, H, D, seed, x_std=3.0, device="cpu"):
+    """h ~ N(0, 1) and weights ~ N(0, x_std²/D), so each projection is ~ N(0, x_std²)."""
+    gen = torch.Generator(device=device).manual_seed(seed)
+    E = len(counts)
+    R = int(sum(counts))
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64)
+    h = torch.randn(R, D, generator=gen, device=device).to(torch.bfloat16)
+    w = torch.empty(E, 2 * H, D, dtype=torch.bfloat16, device=device)
+    for e in range(E):
+        w[e] = (torch.randn(2 * H, D, generator=gen, device=device) * (x_std / D ** 0.5)).to(torch.bfloat16)
+    return h, w, off
+
+
+def run(sg, h, w, off, beta=4.0, lbeta=25.0):
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    x, out = sg.situ_glu_fwd_gateup(h.to(DEV), w.to(DEV), off.to(DEV), status=status, beta=beta, lbeta=lbeta)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    return x, out
+
+
+def check(name, x_gpu_bits, out_gpu_bits, x_exact, xb_ref, mag, beta=4.0, lbeta=25.0):
+    """x: an admissible rounding of the exact projection; out: the oracle's forward at it."""
+    lo = bf16_bits_to_f64(oracle.round_bf16_array(x_exact - ACC_EPS * mag))
+    hi = bf16_bits_to_f64(oracle.round_bf16_array(x_exact + ACC_EPS * mag))
+    xg = bf16_bits_to_f64(x_gpu_bits)
+    admissible = (lo <= xg) & (xg <= hi)
+    n_bad = int((~admissible).sum())
+    if n_bad:
+        idx = np.argwhere(~admissible)[:5]
+        ex = [(tuple(int(k) for k in i), float(xg[tuple(i)]), float(x_exact[tuple(i)]), float(lo[tuple(i)]),
+               float(hi[tuple(i)])) for i in idx]
+        raise AssertionError(f"{name}: {n_bad} x elements are no rounding of the exact projection: {ex}")
+    differs = int((x_gpu_bits != xb_ref).sum())
+    assert differs <= max(8, x_gpu_bits.size // 200), f"{name}: {differs} x elements differ from RNE(exact)"
+    # every bf16 value in [lo, hi] is a correct x; the forward is checked at the one the kernel chose
+    out_ref = oracle.fwd_bf16(np.ascontiguousarray(x_gpu_bits), beta, lbeta)
+    par = Parity(name)
+    par.bf16("out", out_gpu_bits, out_ref)
+    par.assert_ok()
+    return differs
+
+
+CASES = {
+    "one_tile": ([128], 128, 64),
+    "partial_tiles": ([100, 60], 256, 128),
+    "empty_experts": ([0, 300, 1, 129, 0, 77, 0], 384, 192),
+    "real_widths": ([200, 0, 317, 128, 90, 250, 33, 400, 1, 255, 256, 129], 3072, 3584),
+    # H / 128 N-tiles shared by min(8, H / 128) CTAs: 10 over 8 (uneven)
+    "uneven_split": ([300, 77], 1280, 128),
+}
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_gateup_all_rows(sg, name):
+    counts, H, D = CASES[name]
+    h, w, off = make(counts, H, D, seed=len(name))
+    x, out = run(sg, h, w, off)
+    x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy())
+    check("gateup " + name, bits_of(x), bits_of(out), x_exact, xb_ref, mag)
+
+
+@pytest.mark.parametrize("beta,lbeta", [(2.0, 100.0), (4.0, 100.0)])
+def test_gateup_general_scales(sg, beta, lbeta):
+    counts, H, D = [70, 200], 256, 128
+    h, w, off = make(counts, H, D, seed=3)
+    x, out = run(sg, h, w, off, beta, lbeta)
+    x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy(), beta, lbeta)
+    check(f"gateup beta={beta} lbeta={lbeta}", bits_of(x), bits_of(out), x_exact, xb_ref, mag, beta, lbeta)
+
+
+def test_gateup_saturating_inputs(sg):
+    """Projections far into both tails (|x| up to ~80): G -> 4 or -0, L -> +-25."""
+    counts, H, D = [256], 128, 64
+    h, w, off = make(counts, H, D, seed=9, x_std=30.0)
+    x, out = run(sg, h, w, off)
+    x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy())
+    assert float(np.abs(x_exact).max()) > 60.0
+    check("gateup saturating", bits_of(x), bits_of(out), x_exact, xb_ref, mag)
+
+
+def test_gateup_matches_unfused_path(sg):
+    """out of the fused kernel equals situ_glu_fwd applied to the x it wrote, bit for bit: the
+    same forward on the same bf16 values, only without the round trip of x through memory."""
+    counts, H, D = [130, 0, 250], 512, 256
+    h, w, off = make(counts, H, D, seed=4)
+    x, out = run(sg, h, w, off)
+    out2 = sg.situ_glu_fwd(x)
+    torch.cuda.synchronize()
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+
+
+def test_gateup_rejects_unsupported_shapes(sg):
+    h, w, off = make([64], 128, 64, seed=1)
+    with pytest.raises(sg.SituGluError):                  # H = 96 is not a multiple of 128
+        sg.situ_glu_fwd_gateup(h.to(DEV), w.to(DEV)[:, :192].contiguous(), off.to(DEV))
+
+
+@pytest.mark.slow
+def test_gateup_expert_grouped_full_size_sampled(sg):
+    """R = 262144 routed rows grouped by expert over 896 experts (16384 tokens x top-16),
+    H = 3072, D = 3584: the full-size launch, checked on sampled rows."""
+    wl = si.get("expert_grouped_r262144_h3072")
+    _, experts, _ = si.router_rows(wl.tokens, wl.seed, order="expert")
+    counts = np.bincount(experts.numpy(), minlength=si.N_EXPERTS)
+    H, D, E = wl.H, 3584, si.N_EXPERTS
+    gen = torch.Generator(device=DEV).manual_seed(6)
+    h = torch.empty(wl.R, D, dtype=torch.bfloat16, device=DEV)
+    for a in range(0, wl.R, 32768):
+        h[a:a + 32768] = torch.randn(min(32768, wl.R - a), D, generator=gen, device=DEV).to(torch.bfloat16)
+    w = torch.empty(E, 2 * H, D, dtype=torch.bfloat16, device=DEV)
+    for e in range(E):
+        w[e] = (torch.randn(2 * H, D, generator=gen, device=DEV) * (wl.x_std / D ** 0.5)).to(torch.bfloat16)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    x, out = sg.situ_glu_fwd_gateup(h, w, off, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert bool(torch.isfinite(x).all()) and bool(torch.isfinite(out).all())
+    rows = sample_rows(wl.R, n_random=512, seed=12).to(DEV)
+    row_expert = torch.bucketize(rows, off[1:], right=True).cpu().numpy()
+    rows_np = rows.cpu().numpy()
+    xg, og = bits_of(x.index_select(0, rows)), bits_of(out.index_select(0, rows))
+    differs = 0
+    for e in np.unique(row_expert):
+        sel = np.nonzero(row_expert == e)[0]
+        hb = bits_of(h.index_select(0, torch.from_numpy(rows_np[sel]).to(DEV)))
+        x_exact, xb_ref, _, mag = oracle.gateup_fwd(hb, bits_of(w[e]).reshape(1, 2 * H, D),
+                                                    np.array([0, len(sel)], dtype=np.int64))
+        differs += check(f"gateup expert_grouped_r262144 expert {e}", xg[sel], og[sel], x_exact, xb_ref, mag)
+    assert differs <= max(8, xg.size // 200)
+    del h, w, x, out
+    torch.cuda.empty_cache()
