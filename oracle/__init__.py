@@ -52,6 +52,16 @@ def build(force: bool = False) -> str:
     return _LIB
 
 
+class AdamHP(ctypes.Structure):
+    """Adam hyper-parameters and the 1-based step count t (bias corrections 1 - beta^t)."""
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64)]
+
+
+def adam_hp(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=1) -> AdamHP:
+    return AdamHP(lr, beta1, beta2, eps, weight_decay, step)
+
+
 class Oracle:
     """ctypes wrapper over one build of the oracle library."""
 
@@ -86,6 +96,10 @@ class Oracle:
         lib.oracle_round_bf16_array.restype = cint
         lib.oracle_bf16_neighbours.argtypes = [dbl, vp, vp]
         lib.oracle_bf16_neighbours.restype = None
+        lib.oracle_adam_f64.argtypes = [vp, vp, vp, vp, i64, ctypes.POINTER(AdamHP)]
+        lib.oracle_adam_f64.restype = cint
+        lib.oracle_adam_stored.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.POINTER(AdamHP)]
+        lib.oracle_adam_stored.restype = cint
         self.lib = lib
         self.path = path
 
@@ -210,6 +224,29 @@ class Oracle:
         hi = np.zeros(1, dtype=np.uint16)
         self.lib.oracle_bf16_neighbours(float(v), _ptr(lo), _ptr(hi))
         return int(lo[0]), int(hi[0])
+
+    # ---------------- Adam on host-resident optimizer state ----------------
+
+    def adam_f64(self, w, m, v, g, hp: AdamHP):
+        """One textbook Adam step in double on double state; returns new (w, m, v)."""
+        w = np.array(w, dtype=np.float64, copy=True)
+        m = np.array(m, dtype=np.float64, copy=True)
+        v = np.array(v, dtype=np.float64, copy=True)
+        g = np.ascontiguousarray(g, dtype=np.float64)
+        _check(self.lib.oracle_adam_f64(_ptr(w), _ptr(m), _ptr(v), _ptr(g), w.size, ctypes.byref(hp)))
+        return w, m, v
+
+    def adam_stored(self, master, m_bits, v_bits, g, hp: AdamHP):
+        """One Adam step on the stored precisions (fp32 master, bf16 moments, fp32 gradient);
+        returns new (master fp32, m bits, v bits, working-weight bf16 bits)."""
+        master = np.array(master, dtype=np.float32, copy=True)
+        m = np.array(np.asarray(m_bits).view(np.uint16), dtype=np.uint16, copy=True)
+        v = np.array(np.asarray(v_bits).view(np.uint16), dtype=np.uint16, copy=True)
+        g = np.ascontiguousarray(g, dtype=np.float32)
+        w = np.empty(master.shape, dtype=np.uint16)
+        _check(self.lib.oracle_adam_stored(_ptr(master), _ptr(m), _ptr(v), _ptr(g), _ptr(w), master.size,
+                                           ctypes.byref(hp)))
+        return master, m, v, w
 
     # ---------------- fused gate/up projection forward ----------------
 
@@ -394,3 +431,13 @@ def grouped_gateup(h_bits, w_bits, offsets):
 
 def gateup_fwd(h_bits, w_bits, offsets, beta: float = 4.0, lbeta: float = 25.0, nthreads: int = 0):
     return _default().gateup_fwd(h_bits, w_bits, offsets, beta, lbeta, nthreads)
+
+
+# ---------------------------------------------------------------- Adam on host-resident state
+
+def adam_f64(w, m, v, g, hp: AdamHP):
+    return _default().adam_f64(w, m, v, g, hp)
+
+
+def adam_stored(master, m_bits, v_bits, g, hp: AdamHP):
+    return _default().adam_stored(master, m_bits, v_bits, g, hp)

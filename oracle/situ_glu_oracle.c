@@ -440,3 +440,97 @@ int oracle_round_bf16_array(const double* v, uint16_t* out, int64_t n) {
     for (int64_t i = 0; i < n; ++i) out[i] = oracle_round_bf16(v[i]);
     return 0;
 }
+
+/* ===================================================================================
+ * Adam on host-resident optimizer state ([K3-RL] "Memory management" and "Streaming
+ * gradients": the optimizer state lives in host memory as fp32 master weights and two bf16
+ * moment tensors; gradients come from the device, the update is applied chunk by chunk
+ * because Adam treats every parameter independently, and the updated weights go back to the
+ * device as the bf16 working copy).
+ *
+ * The pages name Adam without formulas; the update is the textbook one (Kingma & Ba, with
+ * PyTorch's placement of eps and, when weight_decay > 0, its decoupled AdamW decay):
+ *   w  <- w·(1 - lr·wd)                                  (only when wd > 0)
+ *   m  <- b1·m + (1 - b1)·g
+ *   v  <- b2·v + (1 - b2)·g²
+ *   w  <- w - (lr / (1 - b1^t)) · m / (sqrt(v) / sqrt(1 - b2^t) + eps)
+ *
+ * oracle_adam_f64: that definition in double on double state (the textbook reference).
+ * oracle_adam_stored: the same update on the stored precisions the pages give (fp32 master,
+ * bf16 moments): each step below is one IEEE fp32 operation, rounded to nearest, in this order
+ * (no fused multiply-add), so the bf16 codes of the moments are decided in fp32 like the
+ * product's:
+ *   b1, b2, eps, c1 = 1 - b1, c2 = 1 - b2, s = lr / bc1, r = 1 / sqrt(bc2), d = 1 - lr·wd:
+ *        each formed in double from the double hyper-parameters (bc1 = 1 - b1^t, bc2 = 1 - b2^t)
+ *        and rounded to fp32 once (rounding b2 first and then forming 1 - b2 in fp32 would put
+ *        a 1e-5 relative error on c2 = 0.001)
+ *   w1 = wd > 0 ? fl(w·d) : w
+ *   m1 = fl(fl(b1·m) + fl(c1·g))
+ *   v1 = fl(fl(b2·v) + fl(c2·fl(g·g)))
+ *   q  = fl(fl(sqrt(v1))·r) + eps  -> fl
+ *   w2 = fl(w1 - fl(s·fl(m1 / q)))
+ *   stored: master = w2, m = RNE_bf16(m1), v = RNE_bf16(v1), working weight = RNE_bf16(w2)
+ * =================================================================================== */
+
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+} oracle_adam_hp;
+
+int oracle_adam_f64(double* w, double* m, double* v, const double* g, int64_t n, const oracle_adam_hp* hp) {
+    if (n < 0 || !hp || hp->step < 1) return 1;
+    const double bc1 = 1.0 - pow(hp->beta1, (double)hp->step);
+    const double bc2 = 1.0 - pow(hp->beta2, (double)hp->step);
+    for (int64_t i = 0; i < n; ++i) {
+        if (hp->weight_decay > 0.0) w[i] = w[i] * (1.0 - hp->lr * hp->weight_decay);
+        m[i] = hp->beta1 * m[i] + (1.0 - hp->beta1) * g[i];
+        v[i] = hp->beta2 * v[i] + (1.0 - hp->beta2) * g[i] * g[i];
+        const double denom = sqrt(v[i]) / sqrt(bc2) + hp->eps;
+        w[i] = w[i] - (hp->lr / bc1) * m[i] / denom;
+    }
+    return 0;
+}
+
+static float bf16_bits_to_float(uint16_t b) {
+    uint32_t u = ((uint32_t)b) << 16;
+    float f;
+    memcpy(&f, &u, 4);
+    return f;
+}
+
+int oracle_adam_stored(float* master, uint16_t* m, uint16_t* v, const float* g, uint16_t* w_out, int64_t n,
+                       const oracle_adam_hp* hp) {
+    if (n < 0 || !hp || hp->step < 1) return 1;
+    const double bc1 = 1.0 - pow(hp->beta1, (double)hp->step);
+    const double bc2 = 1.0 - pow(hp->beta2, (double)hp->step);
+    const float b1 = (float)hp->beta1, b2 = (float)hp->beta2, eps = (float)hp->eps;
+    const float c1 = (float)(1.0 - hp->beta1), c2 = (float)(1.0 - hp->beta2);
+    const float s = (float)(hp->lr / bc1);
+    const float r = (float)(1.0 / sqrt(bc2));
+    const float d = (float)(1.0 - hp->lr * hp->weight_decay);
+    const int decay = hp->weight_decay > 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        volatile float t;                 /* one rounding per operation, in this order */
+        float w1 = master[i];
+        if (decay) { t = w1 * d; w1 = t; }
+        float gb = g[i];
+        t = b1 * bf16_bits_to_float(m[i]); float ma = t;
+        t = c1 * gb; float mb = t;
+        t = ma + mb; float m1 = t;
+        t = gb * gb; float gg = t;
+        t = b2 * bf16_bits_to_float(v[i]); float va = t;
+        t = c2 * gg; float vb = t;
+        t = va + vb; float v1 = t;
+        t = sqrtf(v1); float sq = t;
+        t = sq * r; float qa = t;
+        t = qa + eps; float q = t;
+        t = m1 / q; float u = t;
+        t = s * u; float su = t;
+        t = w1 - su; float w2 = t;
+        master[i] = w2;
+        m[i] = oracle_round_bf16((double)m1);
+        v[i] = oracle_round_bf16((double)v1);
+        w_out[i] = oracle_round_bf16((double)w2);
+    }
+    return 0;
+}

@@ -521,3 +521,88 @@ def pin_grouped_gateup(o):
                 G, L, _, _ = o.point(u, v)
                 assert abs(out[r, j] - G * L) <= 1e-14 * max(1.0, abs(G * L))
     assert np.array_equal(x, x2) and np.array_equal(mag, mag2)
+
+
+# ---------------------------------------------------------------- Adam on host-resident state
+
+def _torch_adam_steps(w0, grads, lr, b1, b2, eps, wd):
+    """PyTorch's own Adam / AdamW (float64, CPU, single-tensor path) over a list of gradients."""
+    p = torch.nn.Parameter(torch.tensor(w0, dtype=torch.float64))
+    cls = torch.optim.AdamW if wd > 0 else torch.optim.Adam
+    opt = cls([p], lr=lr, betas=(b1, b2), eps=eps, weight_decay=wd, foreach=False)
+    for g in grads:
+        p.grad = torch.tensor(g, dtype=torch.float64)
+        opt.step()
+    st = opt.state[p]
+    return p.detach().numpy(), st["exp_avg"].numpy(), st["exp_avg_sq"].numpy()
+
+
+def pin_adam_matches_torch(o):
+    """The oracle's textbook Adam (double) equals PyTorch's Adam and AdamW in float64 over several
+    steps, including a large eps (where its placement outside the bias-corrected sqrt matters)."""
+    import oracle as omod
+    rng = np.random.default_rng(31)
+    n = 257
+    for lr, b1, b2, eps, wd in [(1e-3, 0.9, 0.999, 1e-8, 0.0), (3e-2, 0.8, 0.95, 0.1, 0.0),
+                                (1e-2, 0.9, 0.99, 1e-6, 0.1)]:
+        w0 = rng.normal(0, 1, n)
+        grads = [rng.normal(0, 1, n) * 10.0 ** rng.uniform(-3, 1, n) for _ in range(5)]
+        w, m, v = w0.copy(), np.zeros(n), np.zeros(n)
+        for t, g in enumerate(grads, start=1):
+            w, m, v = o.adam_f64(w, m, v, g, omod.adam_hp(lr, b1, b2, eps, wd, t))
+        tw, tm, tv = _torch_adam_steps(w0, grads, lr, b1, b2, eps, wd)
+        assert np.allclose(w, tw, rtol=1e-12, atol=1e-14), (lr, eps, wd)
+        assert np.allclose(m, tm, rtol=1e-12, atol=1e-300) and np.allclose(v, tv, rtol=1e-12, atol=1e-300)
+
+
+def pin_adam_first_step_closed_form(o):
+    """From zero moments at t = 1 the bias corrections cancel (1 - b^1 = 1 - b): m = (1-b1)·g,
+    v = (1-b2)·g², and w moves by exactly lr·g / (|g| + eps), in both precisions."""
+    import oracle as omod
+    g = np.array([0.5, -2.0, 1e-3, 3e4, -7.25e-6, 0.0])
+    lr, eps = 1e-2, 1e-8
+    hp = omod.adam_hp(lr, 0.9, 0.999, eps, 0.0, 1)
+    w, m, v = o.adam_f64(np.ones(g.size), np.zeros(g.size), np.zeros(g.size), g, hp)
+    assert np.allclose(m, 0.1 * g, rtol=1e-15, atol=0) and np.allclose(v, 0.001 * g * g, rtol=1e-14, atol=0)
+    assert np.allclose(w, 1.0 - lr * g / (np.abs(g) + eps), rtol=1e-14, atol=0)
+    ms, mb, vb, wb = o.adam_stored(np.ones(g.size, np.float32), np.zeros(g.size, np.uint16),
+                                   np.zeros(g.size, np.uint16), g.astype(np.float32), hp)
+    ref = 1.0 - lr * g / (np.abs(g) + eps)
+    assert np.all(np.abs(ms - ref) <= 4 * np.spacing(np.float32(1.0)))
+    assert np.array_equal(wb, _bf16_bits(ms))
+
+
+def pin_adam_stored_is_a_rounding_of_f64(o):
+    """One stored-precision step (fp32 arithmetic, bf16 moments) from any state is the double
+    step up to fp32 rounding: the master weight within a few fp32 ulps of the step and of w;
+    the moment codes are round-to-nearest-even of the double moments, except where the double
+    value lies within the fp32 error of a bf16 midpoint; the working weight is RNE of the
+    master. Weight decay on and off, late steps (small bias corrections) too."""
+    import oracle as omod
+    rng = np.random.default_rng(32)
+    n = 4096
+    for t, wd in [(1, 0.0), (7, 0.0), (1000, 0.05), (3, 0.1)]:
+        hp = omod.adam_hp(2e-3, 0.9, 0.999, 1e-8, wd, t)
+        w0 = rng.normal(0, 0.05, n).astype(np.float32)
+        m0 = _bf16_bits(rng.normal(0, 1e-2, n))
+        v0 = _bf16_bits(rng.uniform(0, 1e-3, n))
+        g = (rng.normal(0, 1, n) * 10.0 ** rng.uniform(-4, 0, n)).astype(np.float32)
+        ms, mb, vb, wb = o.adam_stored(w0, m0, v0, g, hp)
+        wd_, md, vd = o.adam_f64(w0.astype(np.float64), _bits_to_f32(m0).astype(np.float64),
+                                  _bits_to_f32(v0).astype(np.float64), g.astype(np.float64), hp)
+        # the update s·m/q rounded in fp32: m = b1·m0 + (1-b1)·g may cancel, so its error scales
+        # with |b1·m0| + |(1-b1)·g|; the rest contributes a few ulps of the update and of w
+        bc1, bc2 = 1 - 0.9 ** t, 1 - 0.999 ** t
+        q = np.sqrt(vd) / np.sqrt(bc2) + 1e-8
+        u_abs = 2e-3 / bc1 * (0.9 * np.abs(_bits_to_f32(m0)) + 0.1 * np.abs(g)) / q
+        big = np.maximum(np.abs(w0).astype(np.float64), np.abs(wd_))
+        tol_w = 4 * np.spacing(big.astype(np.float32)).astype(np.float64) + 8 * 2.0 ** -24 * u_abs
+        assert np.all(np.abs(ms - wd_) <= tol_w)
+        for bits, ref, scale in ((mb, md, 0.9 * np.abs(_bits_to_f32(m0)) + 0.1 * np.abs(g)),
+                                 (vb, vd, 0.999 * _bits_to_f32(v0) + 0.001 * g.astype(np.float64) ** 2)):
+            lo = o.round_bf16_array(ref - 4 * 2.0 ** -24 * scale)
+            hi = o.round_bf16_array(ref + 4 * 2.0 ** -24 * scale)
+            val, vlo, vhi = (_bits_to_f32(x).astype(np.float64) for x in (bits, lo, hi))
+            assert np.all((vlo <= val) & (val <= vhi))
+            assert np.mean(bits == o.round_bf16_array(ref)) > 0.99
+        assert np.array_equal(wb, _bf16_bits(ms))

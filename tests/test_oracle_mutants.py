@@ -29,6 +29,9 @@ PINS = [
     ("fp8_bwd", _pins.pin_fp8_backward_is_backward_of_dequantized),
     ("round_bf16", _pins.pin_round_bf16),
     ("gateup", _pins.pin_grouped_gateup),
+    ("adam_torch", _pins.pin_adam_matches_torch),
+    ("adam_first_step", _pins.pin_adam_first_step_closed_form),
+    ("adam_stored", _pins.pin_adam_stored_is_a_rounding_of_f64),
 ]
 
 MUTANTS = {
@@ -75,6 +78,21 @@ MUTANTS = {
                                 "    double ulp = ldexp(1.0, ex - 7);\n    double q = a / ulp;"),
     "bf16_overflow_at_max": ("uint16_t b = r > ldexp(255.0, 120) ? 0x7F80", "uint16_t b = r >= ldexp(255.0, 120) ? 0x7F80"),
     "bf16_sign_dropped": ("return (uint16_t)((signbit(v) ? 0x8000 : 0) | b);", "return b;"),
+    # Adam on host-resident state
+    "adam_f64_no_bc2": ("const double denom = sqrt(v[i]) / sqrt(bc2) + hp->eps;",
+                        "const double denom = sqrt(v[i]) + hp->eps;"),
+    "adam_f64_ascent": ("w[i] = w[i] - (hp->lr / bc1) * m[i] / denom;", "w[i] = w[i] + (hp->lr / bc1) * m[i] / denom;"),
+    "adam_f64_coupled_decay": ("if (hp->weight_decay > 0.0) w[i] = w[i] * (1.0 - hp->lr * hp->weight_decay);",
+                               "if (hp->weight_decay > 0.0) w[i] = w[i] * (1.0 - hp->weight_decay);"),
+    "adam_no_bc1": ("const float s = (float)(hp->lr / bc1);", "const float s = (float)(hp->lr);"),
+    "adam_no_sqrt": ("t = sqrtf(v1); float sq = t;", "t = v1; float sq = t;"),
+    "adam_eps_inside_sqrt": ("        t = sqrtf(v1); float sq = t;\n        t = sq * r; float qa = t;\n        t = qa + eps; float q = t;",
+                             "        t = sqrtf(v1 + eps); float sq = t;\n        t = sq * r; float qa = t;\n        t = qa; float q = t;"),
+    "adam_betas_swapped": ("t = b1 * bf16_bits_to_float(m[i]); float ma = t;", "t = b2 * bf16_bits_to_float(m[i]); float ma = t;"),
+    "adam_g_not_squared": ("t = gb * gb; float gg = t;", "t = gb; float gg = t;"),
+    "adam_decay_ignored": ("if (decay) { t = w1 * d; w1 = t; }", "(void)d;"),
+    "adam_working_weight_stale": ("w_out[i] = oracle_round_bf16((double)w2);", "w_out[i] = oracle_round_bf16((double)w1);"),
+    "adam_m_without_gradient": ("m[i] = oracle_round_bf16((double)m1);", "m[i] = oracle_round_bf16((double)ma);"),
 }
 
 

@@ -100,3 +100,15 @@ def test_round_bf16():
 
 def test_grouped_gateup():
     _pins.pin_grouped_gateup(oracle)
+
+
+def test_adam_matches_torch():
+    _pins.pin_adam_matches_torch(oracle)
+
+
+def test_adam_first_step_closed_form():
+    _pins.pin_adam_first_step_closed_form(oracle)
+
+
+def test_adam_stored_is_a_rounding_of_f64():
+    _pins.pin_adam_stored_is_a_rounding_of_f64(oracle)
