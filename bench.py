@@ -66,8 +66,11 @@ def parse_args(argv=None):
     ap.add_argument("--no-fp8", action="store_true", help="skip the FP8 saved-x variant's timing")
     ap.add_argument("--no-dgrad", action="store_true", help="skip the fused dgrad GEMM's timing")
     ap.add_argument("--no-gateup", action="store_true", help="skip the fused gate/up GEMM's timing")
+    ap.add_argument("--no-adam", action="store_true", help="skip the streamed host Adam step's timing")
     ap.add_argument("--only-dgrad", action="store_true", help="time only the fused dgrad GEMM (profiling runs)")
     ap.add_argument("--only-gateup", action="store_true", help="time only the fused gate/up GEMM (profiling runs)")
+    ap.add_argument("--only-adam", action="store_true", help="time only the streamed host Adam step")
+    ap.add_argument("--adam-params", type=int, default=1 << 28, help="parameters of the Adam leg")
     ap.add_argument("--gemm-rows", type=int, default=None, help="rows split evenly over --gemm-experts")
     ap.add_argument("--gemm-experts", type=int, default=None)
     ap.add_argument("--rows", type=int, default=None, help="override R (for small profiling runs)")
@@ -285,6 +288,8 @@ def run_gemm_only(args):
         line["gateup_fused"] = time_gateup(sg, dev, args.steps, args.warmup, peak, rows=args.gemm_rows,
                                            experts=args.gemm_experts)
         ok &= line["gateup_fused"]["status"] == 0
+    if args.only_adam:
+        line["adam_stream"] = time_adam(sg, dev, args.steps, n=args.adam_params)
     print(json.dumps(line), flush=True)
     return 0 if ok else 1
 
@@ -371,6 +376,7 @@ def run_native(args):
     fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
     dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak)
     gateup = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak)
+    adam = None if args.no_adam else time_adam(sg, dev, 3, n=args.adam_params)
 
     traffic = None
     if NCU_TRAFFIC["source_sha256"] == kernel_source_hash() and NCU_TRAFFIC["bwd_bytes_per_row"]:
@@ -426,6 +432,7 @@ def run_native(args):
         "fp8_saved_x": fp8,
         "dgrad_fused": dgrad,
         "gateup_fused": gateup,
+        "adam_stream": adam,
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -593,6 +600,98 @@ def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, exp
     return res
 
 
+def time_adam(sg, dev, steps, n=1 << 28, chunk=1 << 24, nslots=2, seed=7):
+    """Adam on host-resident state, streamed (the streaming-gradients design) against the one-big-
+    transfer baseline it replaces, on n parameters: device fp32 gradients, host fp32 master + bf16
+    moments, device bf16 working weights. Also times each leg alone (gradient D2H, weight H2D, the
+    host update on resident data) to give the overlap roofline: a perfectly overlapped step takes
+    max(D2H + H2D on the one copy stream, host update)."""
+    import time
+
+    import numpy as np
+    import torch
+    gen = torch.Generator(device=dev).manual_seed(seed)
+    grad = torch.randn(n, generator=gen, device=dev) * 1e-3
+    weight = torch.zeros(n, dtype=torch.bfloat16, device=dev)
+    master = torch.zeros(n, dtype=torch.float32).normal_(0, 0.02)
+    m = torch.zeros(n, dtype=torch.bfloat16)
+    v = torch.zeros(n, dtype=torch.bfloat16)
+    staging = pinned_like(torch.empty(sg.adam_staging_bytes(chunk, nslots), dtype=torch.uint8))
+    stream = torch.cuda.current_stream(dev)
+    threads = len(os.sched_getaffinity(0))
+
+    def streamed(step):
+        sg.situ_adam_stream_step(grad, weight, master, m, v, sg.adam_params(step=step), staging, chunk, nslots,
+                                 threads, stream)
+
+    for i in range(2):                                    # warm-up (page faults, thread start)
+        streamed(i + 1)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        streamed(i + 3)
+    t_stream = (time.perf_counter() - t0) / steps
+
+    # the baseline: one parameter-sized fp32 host gradient buffer, one transfer each way
+    gbuf = pinned_like(torch.empty(n, dtype=torch.float32))
+    wbuf = pinned_like(torch.empty(n, dtype=torch.bfloat16))
+
+    def one_big(step):
+        gbuf.copy_(grad, non_blocking=True)
+        torch.cuda.synchronize(dev)
+        sg.situ_adam_update_host(master, m, v, gbuf, wbuf, sg.adam_params(step=step), threads)
+        weight.copy_(wbuf, non_blocking=True)
+        torch.cuda.synchronize(dev)
+
+    one_big(1)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        one_big(i + 2)
+    t_big = (time.perf_counter() - t0) / steps
+
+    # legs alone
+    def timed(fn, reps=3):
+        fn()
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            fn()
+        torch.cuda.synchronize(dev)
+        return (time.perf_counter() - t0) / reps
+    t_d2h = timed(lambda: gbuf.copy_(grad, non_blocking=True))
+    t_h2d = timed(lambda: weight.copy_(wbuf, non_blocking=True))
+    t_upd = timed(lambda: sg.situ_adam_update_host(master, m, v, gbuf, wbuf, sg.adam_params(step=9), threads))
+    ideal = max(t_d2h + t_h2d, t_upd)
+    # host memory: a multi-threaded copy of 1 GiB (read + write bytes), the denominator of the
+    # host-memory roofline; the streamed step moves 28 B per parameter through host memory
+    # (update: read g 4, master 4, m 2, v 2; write master 4, m 2, v 2, weight slot 2; DMA: the
+    # gradient slot written 4, the weight slot read 2)
+    torch.set_num_threads(threads)
+    src = torch.empty(1 << 28, dtype=torch.float32).fill_(1.0)
+    dst = torch.empty_like(src)
+    t_copy = timed(lambda: dst.copy_(src), reps=5)
+    host_peak = 2 * src.numel() * 4 / t_copy / 1e9
+    del src, dst
+    host_gbs = 28 * n / t_stream / 1e9
+    for t in (staging, gbuf, wbuf):
+        torch.cuda.cudart().cudaHostUnregister(t.data_ptr())
+    del grad, weight
+    torch.cuda.empty_cache()
+    return {"params": n, "chunk": chunk, "nslots": nslots, "host_threads": threads,
+            "ms": t_stream * 1e3, "params_per_s": n / t_stream,
+            "one_big_transfer_ms": t_big * 1e3, "one_big_transfer_params_per_s": n / t_big,
+            "host_bytes_per_param": {"streamed": 8 + sg.adam_staging_bytes(chunk, nslots) / n, "one_big_transfer": 12},
+            "legs_ms": {"grad_d2h": t_d2h * 1e3, "weight_h2d": t_h2d * 1e3, "host_update": t_upd * 1e3},
+            "link_GB_s": {"d2h": 4 * n / t_d2h / 1e9, "h2d": 2 * n / t_h2d / 1e9},
+            "host_update_params_per_s": n / t_upd,
+            "roofline": {"bound": "host_memory", "achieved": host_gbs, "peak": host_peak, "unit": "GB/s",
+                         "frac": host_gbs / host_peak, "bytes_per_param": 28,
+                         "peak_source": "measured here: multi-threaded host copy of 1 GiB, read + write bytes"},
+            "overlap": {"slowest_leg": "host_update" if t_upd >= t_d2h + t_h2d else "host_link",
+                        "ideal_ms": ideal * 1e3, "frac": ideal / t_stream},
+            "timing": "host wall clock per step (the step returns when every chunk's weights are on the device)"}
+
+
 def pinned_like(t):
     """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size, touched).
 
@@ -694,7 +793,7 @@ def main(argv=None):
     args = parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
-    if args.only_dgrad or args.only_gateup:
+    if args.only_dgrad or args.only_gateup or args.only_adam:
         return run_gemm_only(args)
     return run_native(args)
 

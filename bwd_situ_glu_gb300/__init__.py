@@ -29,7 +29,9 @@ INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("situ_glu.cu", "situ_glu_fp8.cu", "situ_glu_dgrad.cu",
-                                             "situ_glu_gateup.cu")]
+                                             "situ_glu_gateup.cu", "situ_adam.cu")]
+# per-source extra flags: the host Adam update is a fixed sequence of IEEE fp32 operations
+SOURCE_FLAGS = {"situ_adam.cu": ["-Xcompiler", "-ffp-contract=off,-fno-fast-math,-fno-math-errno"]}
 DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h",
                                                      "situ_tc.cuh")] + [os.path.join(INCLUDE, "situ_glu.h")]
 
@@ -43,6 +45,16 @@ STATUS_OK, STATUS_INVALID_ARG, STATUS_OVERLAP, STATUS_CUDA_ERROR = 0, 1, 2, 3
 
 _lock = threading.Lock()
 _lib = None
+
+
+class AdamParams(ctypes.Structure):
+    """situ_adam_params: Adam hyper-parameters and the 1-based step count of the update."""
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double), ("beta2", ctypes.c_double),
+                ("eps", ctypes.c_double), ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64)]
+
+
+def adam_params(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0, step=1) -> AdamParams:
+    return AdamParams(lr, beta1, beta2, eps, weight_decay, step)
 
 
 class SituGluError(RuntimeError):
@@ -68,7 +80,8 @@ def build(force: bool = False, verbose: bool = False) -> str:
             objs, procs = [], []
             for src in SOURCES:
                 obj = os.path.join(LIB_DIR, os.path.basename(src) + tag + ".o")
-                cmd = [_nvcc(), *[f for f in NVCC_FLAGS if f != "-shared"], "-I", INCLUDE, "-c", "-o", obj, src]
+                cmd = [_nvcc(), *[f for f in NVCC_FLAGS if f != "-shared"],
+                       *SOURCE_FLAGS.get(os.path.basename(src), []), "-I", INCLUDE, "-c", "-o", obj, src]
                 if verbose:
                     cmd.insert(1, "-Xptxas=-v")
                 objs.append(obj)
@@ -108,6 +121,11 @@ def load():
     lib.situ_glu_bwd_router_dgrad.restype = cint
     lib.situ_glu_fwd_gateup.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, f32, f32, vp]
     lib.situ_glu_fwd_gateup.restype = cint
+    lib.situ_adam_update_host.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.POINTER(AdamParams), cint]
+    lib.situ_adam_update_host.restype = cint
+    lib.situ_adam_stream_step.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.POINTER(AdamParams), vp, i64, cint, cint,
+                                          vp]
+    lib.situ_adam_stream_step.restype = cint
     lib.situ_glu_status_string.argtypes = [cint]
     lib.situ_glu_status_string.restype = ctypes.c_char_p
     lib.situ_glu_last_cuda_error.argtypes = []
@@ -334,10 +352,62 @@ def situ_glu_fwd_gateup(h, w_gate_up, expert_offsets, x=None, out=None, status=N
     return x, out
 
 
+def _host_ptr(t, dtype, n, name):
+    """Pointer of a contiguous CPU tensor or numpy array of `n` elements of `dtype` (torch dtype)."""
+    import numpy as np
+    import torch
+    if isinstance(t, np.ndarray):
+        want = {torch.float32: np.float32, torch.bfloat16: np.uint16, torch.uint8: np.uint8}[dtype]
+        if t.dtype != want or t.size != n or not t.flags["C_CONTIGUOUS"]:
+            raise ValueError(f"{name}: expected a contiguous {want.__name__} array of {n} elements")
+        return t.ctypes.data
+    if t.device.type != "cpu" or t.dtype != dtype or t.numel() != n or not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous CPU {dtype} tensor of {n} elements")
+    return t.data_ptr()
+
+
+def situ_adam_update_host(master, m, v, g, w_out, params: AdamParams, nthreads: int = 0):
+    """One Adam step on host memory (master fp32, m / v bf16 updated in place; g fp32 read;
+    w_out bf16 written). Accepts CPU tensors or numpy arrays (bf16 as uint16 bits)."""
+    import torch
+    n = master.numel() if hasattr(master, "numel") else master.size
+    _check(load().situ_adam_update_host(_host_ptr(master, torch.float32, n, "master"),
+                                        _host_ptr(m, torch.bfloat16, n, "m"), _host_ptr(v, torch.bfloat16, n, "v"),
+                                        _host_ptr(g, torch.float32, n, "g"),
+                                        _host_ptr(w_out, torch.bfloat16, n, "w_out"), n, ctypes.byref(params),
+                                        int(nthreads)))
+
+
+def adam_staging_bytes(chunk: int, nslots: int) -> int:
+    return nslots * chunk * 6
+
+
+def situ_adam_stream_step(grad, weight, master, m, v, params: AdamParams, staging, chunk: int, nslots: int = 2,
+                          nthreads: int = 0, stream=None):
+    """The streamed Adam step: device fp32 gradients `grad` [n] in, device bf16 `weight` [n]
+    overwritten with the new working weights, host master fp32 / m, v bf16 updated in place;
+    `staging` page-locked host memory of adam_staging_bytes(chunk, nslots) bytes."""
+    import torch
+    n = grad.numel()
+    _need(grad, torch.float32, (n,), "grad")
+    _need(weight, torch.bfloat16, (n,), "weight")
+    nb = adam_staging_bytes(chunk, nslots)
+    sp = _host_ptr(staging, torch.uint8, staging.numel() if hasattr(staging, "numel") else staging.size, "staging")
+    if (staging.numel() if hasattr(staging, "numel") else staging.size) < nb:
+        raise ValueError(f"staging: needs {nb} bytes")
+    with torch.cuda.device(grad.device):
+        _check(load().situ_adam_stream_step(grad.data_ptr(), weight.data_ptr(),
+                                            _host_ptr(master, torch.float32, n, "master"),
+                                            _host_ptr(m, torch.bfloat16, n, "m"), _host_ptr(v, torch.bfloat16, n, "v"),
+                                            n, ctypes.byref(params), sp, int(chunk), int(nslots), int(nthreads),
+                                            _stream_handle(stream, grad.device)))
+
+
 __all__ = [
     "build", "load", "version", "status_string", "SituGluError",
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
     "situ_glu_bwd_router_dgrad", "situ_glu_fwd_gateup",
+    "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
     "LIB_PATH", "INCLUDE",
 ]

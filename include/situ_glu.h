@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 2
+#define SITU_GLU_VERSION_MINOR 3
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -220,6 +220,53 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
 int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* expert_offsets,
                         int64_t E, void* x, void* out, int* status, int64_t R, int64_t H,
                         int64_t D, float beta, float lbeta, cudaStream_t stream);
+
+/* ---------------------------------------------------------------------------------------
+ * Adam on host-resident optimizer state, streamed chunk by chunk.
+ *
+ * "Frontier-scale RL with Kimi K3", sections "Memory management" and "Streaming gradients": the
+ * optimizer state lives in host memory (fp32 master weights, two bf16 moment tensors); the
+ * device's gradients are brought to the host and the updated weights go back as the bf16
+ * working copy. Instead of one parameter-sized fp32 host gradient buffer (12 bytes of host
+ * memory per parameter), the update runs chunk by chunk with the transfers of the next chunks
+ * in flight: 8 bytes per parameter plus nslots chunk-sized staging slots.
+ *
+ * One step per element, as single IEEE fp32 operations in this order (no fused multiply-add):
+ *   constants formed in double from the fields below and rounded to fp32 once:
+ *     b1, b2, eps, c1 = 1 - beta1, c2 = 1 - beta2, s = lr / (1 - beta1^step),
+ *     r = 1 / sqrt(1 - beta2^step), d = 1 - lr * weight_decay
+ *   w1 = weight_decay > 0 ? w * d : w          (decoupled weight decay, as PyTorch's AdamW)
+ *   m1 = b1*m + c1*g;   v1 = b2*v + c2*(g*g);   q = sqrt(v1)*r + eps;   w2 = w1 - s*(m1/q)
+ *   stored: master = w2; m, v, working weight = bf16(m1), bf16(v1), bf16(w2), rounded to nearest
+ *   even (NaN -> 0x7FC0).
+ * --------------------------------------------------------------------------------------- */
+typedef struct {
+    double lr;            /* >= 0, finite */
+    double beta1, beta2;  /* in [0, 1) */
+    double eps;           /* > 0 */
+    double weight_decay;  /* >= 0; 0 = plain Adam */
+    int64_t step;         /* 1-based step count t of this update (bias corrections 1 - beta^t) */
+} situ_adam_params;
+
+/* One step over n parameters, all in host memory: master fp32 [n], m and v bf16 [n] updated in
+ * place, g fp32 [n] read, w_out bf16 [n] written with the new working weights. nthreads host
+ * threads (<= 0: the CPUs this process may run on). No CUDA call. Buffers may not overlap
+ * (SITU_GLU_OVERLAP); fp32 pointers 4-byte and bf16 pointers 2-byte aligned. */
+int situ_adam_update_host(float* master, void* m, void* v, const float* g, void* w_out, int64_t n,
+                          const situ_adam_params* hp, int nthreads);
+
+/* The streamed step: grad_dev device fp32 [n] (read), weight_dev device bf16 [n] (overwritten with
+ * the new working weights), master / m / v host as above (any host memory), staging page-locked
+ * host memory of nslots * chunk * 6 bytes (16-byte aligned; nslots fp32 gradient slots, then
+ * nslots bf16 weight slots), chunk elements per transfer (a positive multiple of 64),
+ * 2 <= nslots <= 64. The copies run on `stream` in order after the work already queued there
+ * (so after the kernels that produced the gradients), gradient chunk c + nslots in flight while
+ * chunk c is updated by nthreads host threads; returns when every chunk's weights are on the
+ * device. Creates and destroys 2*nslots CUDA events per call; allocates no memory. On a CUDA
+ * error (SITU_GLU_CUDA_ERROR) a prefix of the chunks may have been updated. */
+int situ_adam_stream_step(const float* grad_dev, void* weight_dev, float* master, void* m, void* v,
+                          int64_t n, const situ_adam_params* hp, void* staging, int64_t chunk,
+                          int nslots, int nthreads, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code (unknown codes included). */
 const char* situ_glu_status_string(int status);

@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10200
+    assert sg.version() == 10300
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
