@@ -41,10 +41,13 @@ constexpr int COLS_PER_WARP = BN / EPW;      // accumulator columns of one job a
 constexpr int CPJ = COLS_PER_WARP / CW;      // chunks per job per epilogue warp
 constexpr int XV = CW / 16;                  // 32-byte vectors (16 bf16) per half-row per chunk
 static_assert(CPJ >= 2 && CPJ % 2 == 0, "the x prefetch alternates two register buffers");
-constexpr int MAX_SPLIT = 8;                 // largest cluster (portable size)
 constexpr int DGRAD_SPLIT = 4;               // CTAs per cluster sharing an M-tile (each every 4th N-tile)
+constexpr int MAX_SPLIT = DGRAD_SPLIT;
 // extra shared memory: dp_part [EPW][BM] | dp_cl [2][MAX_SPLIT][BM] | dp_full[2], dp_free[2]
 constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 16 + EPW * BM * 4 + 2 * MAX_SPLIT * BM * 4 + 4 * 8;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
+// dx leaves in per-thread 32-byte stores: staging it in shared memory for TMA tensor stores (as the
+// gate/up epilogue does) was measured slower here, where the epilogue also has x loads in flight.
 
 // ---------------------------------------------------------------- the kernel
 

@@ -36,18 +36,22 @@ using namespace situ_tc;
 
 constexpr int HN = BN / 2;                   // column pairs per job (128 gate + 128 linear columns)
 constexpr int EPW = 2;                       // epilogue warps per 32-lane TMEM quadrant
-constexpr int CW = 32;                       // column pairs per chunk
+constexpr int CW = 16;                       // column pairs per chunk
 constexpr int NUM_EPI_THREADS = 4 * EPW * 32;
 constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;  // warp 0 TMA, warp 1 MMA, then the epilogue
 constexpr int PAIRS_PER_WARP = HN / EPW;
 constexpr int CPJ = PAIRS_PER_WARP / CW;     // chunks per job per epilogue warp
 static_assert(CPJ >= 1 && PAIRS_PER_WARP % CW == 0, "whole chunks per warp");
-constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 16;
+constexpr int STAGE_TILE = 32 * CW * 2;      // one 32-row x CW-column bf16 output tile in shared memory
+constexpr int STAGE_BYTES_EPI = 4 * EPW * 3 * STAGE_TILE;   // [warp][x gate, x linear, out]
+constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 128 + STAGE_BYTES_EPI;
+static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int CSPLIT = 8;                    // CTAs sharing an M-tile (each every 8th N-tile)
 
 template <bool BETA4>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gateup_fwd_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
+                      const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_out,
                       const int64_t* __restrict__ offsets, uint16_t* __restrict__ x, uint16_t* __restrict__ out,
                       int* __restrict__ status, int E, int64_t R, int64_t H, int KB, int csplit, Coef c) {
     extern __shared__ uint8_t smem_raw[];
@@ -78,6 +82,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int slot = (warp - 2) >> 2;
         const int lrow = quad * 32 + lane;
         const uint32_t t_lane = (uint32_t)(quad * 32) << 16;
+        uint8_t* stage = (uint8_t*)(((uintptr_t)sm.extra + 127) & ~(uintptr_t)127);
+        uint8_t* st_g = stage + (warp - 2) * 3 * STAGE_TILE;   // this warp's x gate, x linear, out tiles
+        uint8_t* st_l = st_g + STAGE_TILE;
+        uint8_t* st_o = st_l + STAGE_TILE;
+        bool stores_pending = false;                            // lane 0 has TMA stores in flight
         int job = 0;
         bool ok = true;
         for (int t = sc.t0; t < T; t += sc.tstep) {
@@ -86,6 +95,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tile_rows(sm.tile_start, offsets, E, R, t, e, row0, row_end);
             const int64_t row = row0 + lrow;
             const bool valid = ok && row >= 0 && row < row_end;
+            // all 32 rows of this warp's quadrant belong to the expert: x and out leave through TMA stores
+            const bool full_quad = row0 + quad * 32 + 31 < row_end;
             uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * PAIRS_PER_WARP;
             uint16_t* outr = out + (valid ? row : 0) * H + slot * PAIRS_PER_WARP;
             for (int nt = sc.n0; nt < NT; nt += sc.nstep, ++job) {
@@ -107,28 +118,53 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         tc_fence_before();
                         mbar_arrive(&bars->tempty[acc]);       // accumulator may be overwritten
                     }
+                    static_assert(CW == 16, "one 32-byte vector per output row per chunk");
+                    Vec<8> xg, xl, o;
                     if (ok && valid) {
-                        const int64_t j0 = (int64_t)nt * HN + k * CW;
 #pragma unroll
-                        for (int v = 0; v < CW / 16; ++v) {
-                            Vec<8> xg, xl, o;
-#pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const int q = 16 * v + 2 * i;
-                                xg.w[i] = pack_bf16x2(__uint_as_float(gr[q]), __uint_as_float(gr[q + 1]));
-                                xl.w[i] = pack_bf16x2(__uint_as_float(lr[q]), __uint_as_float(lr[q + 1]));
-                                const float a0 = situ::fwd<BETA4>(bf16_lo(xg.w[i]), bf16_lo(xl.w[i]), c);
-                                const float a1 = situ::fwd<BETA4>(bf16_hi(xg.w[i]), bf16_hi(xl.w[i]), c);
-                                o.w[i] = pack_bf16x2(a0, a1);
-                            }
-                            st_stream<8>((Vec<8>*)(xr + j0 + 16 * v), xg);
-                            st_stream<8>((Vec<8>*)(xr + H + j0 + 16 * v), xl);
-                            st_stream<8>((Vec<8>*)(outr + j0 + 16 * v), o);
+                        for (int i = 0; i < 8; ++i) {
+                            xg.w[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
+                            xl.w[i] = pack_bf16x2(__uint_as_float(lr[2 * i]), __uint_as_float(lr[2 * i + 1]));
+                            const float a0 = situ::fwd<BETA4>(bf16_lo(xg.w[i]), bf16_lo(xl.w[i]), c);
+                            const float a1 = situ::fwd<BETA4>(bf16_hi(xg.w[i]), bf16_hi(xl.w[i]), c);
+                            o.w[i] = pack_bf16x2(a0, a1);
                         }
+                    }
+                    const int64_t jl = (int64_t)nt * HN + k * CW;                        // within the slice
+                    const int64_t j0 = jl + slot * PAIRS_PER_WARP;                       // column in [0, H)
+                    if (ok && full_quad) {
+                        // the warp's 32 rows x CW columns of x (both halves) and of out: staged, then
+                        // one TMA store each
+                        if (stores_pending) {
+                            if (lane == 0) bulk_wait_read_all();     // the previous tiles have been read out
+                            __syncwarp();
+                        }
+                        st_shared_v4(st_g + lane * 32, xg.w[0], xg.w[1], xg.w[2], xg.w[3]);
+                        st_shared_v4(st_g + lane * 32 + 16, xg.w[4], xg.w[5], xg.w[6], xg.w[7]);
+                        st_shared_v4(st_l + lane * 32, xl.w[0], xl.w[1], xl.w[2], xl.w[3]);
+                        st_shared_v4(st_l + lane * 32 + 16, xl.w[4], xl.w[5], xl.w[6], xl.w[7]);
+                        st_shared_v4(st_o + lane * 32, o.w[0], o.w[1], o.w[2], o.w[3]);
+                        st_shared_v4(st_o + lane * 32 + 16, o.w[4], o.w[5], o.w[6], o.w[7]);
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (lane == 0) {
+                            const int r0q = (int)(row0 + quad * 32);
+                            tma_store_2d(&map_x, (int)j0, r0q, st_g);
+                            tma_store_2d(&map_x, (int)(H + j0), r0q, st_l);
+                            tma_store_2d(&map_out, (int)j0, r0q, st_o);
+                            bulk_commit();
+                        }
+                        stores_pending = true;
+                    } else if (ok && valid) {
+                        // a quadrant crossing the expert's end: only this row, from registers
+                        st_stream<8>((Vec<8>*)(xr + jl), xg);
+                        st_stream<8>((Vec<8>*)(xr + H + jl), xl);
+                        st_stream<8>((Vec<8>*)(outr + jl), o);
                     }
                 }
             }
         }
+        if (lane == 0 && stores_pending) bulk_wait_all();           // every x and out tile written
     }
 
     pipeline_teardown(tmem);
@@ -163,6 +199,9 @@ int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* exp
     CUtensorMap map_h, map_w;
     if (!make_map(&map_h, h, (uint64_t)R, (uint64_t)D, BM)) return cuda_fail(cudaErrorInvalidValue);
     if (!make_map(&map_w, w_gate_up, (uint64_t)(E * 2 * H), (uint64_t)D, HN)) return cuda_fail(cudaErrorInvalidValue);
+    CUtensorMap map_x, map_out;
+    if (!make_map(&map_x, x, (uint64_t)R, (uint64_t)(2 * H), 32, CW, false)) return cuda_fail(cudaErrorInvalidValue);
+    if (!make_map(&map_out, out, (uint64_t)R, (uint64_t)H, 32, CW, false)) return cuda_fail(cudaErrorInvalidValue);
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
@@ -173,7 +212,8 @@ int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* exp
     const int csplit = NT < CSPLIT ? NT : CSPLIT;
     int grid = 0;
     if ((e = (cudaError_t)persistent_grid(R, E, csplit, &grid)) != cudaSuccess) return cuda_fail(e);
-    kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_h, map_w, expert_offsets, (uint16_t*)x, (uint16_t*)out,
+    kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_h, map_w, map_x, map_out, expert_offsets, (uint16_t*)x,
+                                                      (uint16_t*)out,
                                                       status, (int)E, R, H, (int)(D / BK), csplit, c);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);

@@ -44,7 +44,7 @@ constexpr int A_BYTES = BM * BK * 2;         // 16 KB
 constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 columns
-constexpr int MAX_EXPERTS = 4096;
+constexpr int MAX_EXPERTS = 1024;           // the per-CTA tile prefix lives in shared memory
 constexpr uint32_t WAIT_LIMIT = 1u << 22;    // polls of a try_wait before giving up (~1-2 s)
 
 struct alignas(8) Barriers {
@@ -149,6 +149,31 @@ __device__ __forceinline__ uint64_t make_policy() {
 // B tiles (weights, read by the few M-tiles of their expert at nearly the same time).
 constexpr L2Hint kHintA = L2Hint::normal;
 constexpr L2Hint kHintB = L2Hint::normal;
+
+// ---------------------------------------------------------------- TMA stores (epilogue output tiles)
+
+// Order this thread's generic-proxy shared-memory writes before later async-proxy (TMA) reads.
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Store a box of a 2-D tensor map from shared memory (bulk-group completion).
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* map, int c0, int c1, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(map), "r"(c0),
+                 "r"(c1), "r"(smem_addr(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Wait until the committed bulk stores of this thread have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Wait until the committed bulk stores of this thread are complete.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+__device__ __forceinline__ void st_shared_v4(void* p, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(smem_addr(p)), "r"(a), "r"(b), "r"(c), "r"(d)
+                 : "memory");
+}
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -469,18 +494,20 @@ inline EncodeTiled encode_fn() {
     return fn;
 }
 
-// 2-D bf16 tensor map: rows x cols (cols contiguous), box of box_rows x 64 columns, 128-byte swizzle.
-// Rows past the end read as zero.
-inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// 2-D bf16 tensor map: rows x cols (cols contiguous), box of box_rows x box_cols. Operand tiles use
+// 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect; epilogue output
+// tiles are unswizzled. Rows past the end read as zero and are not written.
+inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                     uint32_t box_cols = BK, bool swizzle128 = true) {
     EncodeTiled fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
     const cuuint64_t strides[1] = {cols * 2};
-    const cuuint32_t box[2] = {(cuuint32_t)BK, box_rows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Launch of a persistent kernel as clusters of csplit CTAs (csplit = 1: plain CTAs): as many

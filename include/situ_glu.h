@@ -179,7 +179,7 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
  *   p, dx, dp  as for situ_glu_bwd_router
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.
- *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 4096, R < 2^31, E*H < 2^31
+ *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 1024, R < 2^31, E*H < 2^31
  *   Pointers to dy and w_down_t must be 16-byte aligned (TMA), to x and dx 32-byte aligned
  *   (32-byte vector access).
  * Returns SITU_GLU_INVALID_ARG for shapes or alignments outside these limits (there is no
@@ -212,7 +212,7 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
  *   out        device, bf16 [R,H], written: SiTU-GLU of x
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then x and out are incomplete). Zero it beforehand.
- *   R, H, D, E sizes: H % 128 == 0, D % 64 == 0, 1 <= E <= 4096, R < 2^31, E*2H < 2^31
+ *   R, H, D, E sizes: H % 128 == 0, D % 64 == 0, 1 <= E <= 1024, R < 2^31, E*2H < 2^31
  *   Pointers to h and w_gate_up must be 16-byte aligned (TMA), to x and out 32-byte aligned.
  * x and out may not overlap each other or any input (SITU_GLU_OVERLAP). Returns
  * SITU_GLU_INVALID_ARG for shapes or alignments outside these limits.
