@@ -29,7 +29,7 @@ INCLUDE = os.path.join(_ROOT, "include")
 LIB_DIR = os.path.join(_HERE, "_lib")
 LIB_PATH = os.path.join(LIB_DIR, "libsitu_glu.so")
 SOURCES = [os.path.join(CSRC, n) for n in ("situ_glu.cu", "situ_glu_fp8.cu", "situ_glu_dgrad.cu",
-                                             "situ_glu_gateup.cu", "situ_adam.cu")]
+                                             "situ_glu_gateup.cu", "situ_adam.cu", "situ_glu_selftest.cu")]
 # per-source extra flags: the host Adam update is a fixed sequence of IEEE fp32 operations
 SOURCE_FLAGS = {"situ_adam.cu": ["-Xcompiler", "-ffp-contract=off,-fno-fast-math,-fno-math-errno"]}
 DEPENDS = SOURCES + [os.path.join(CSRC, n) for n in ("situ_math.cuh", "situ_device.cuh", "situ_host.h",
@@ -121,6 +121,8 @@ def load():
     lib.situ_glu_bwd_router_dgrad.restype = cint
     lib.situ_glu_fwd_gateup.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, f32, f32, vp]
     lib.situ_glu_fwd_gateup.restype = cint
+    lib.situ_glu_selftest_wait_timeout.argtypes = [vp, vp, vp]
+    lib.situ_glu_selftest_wait_timeout.restype = cint
     lib.situ_adam_update_host.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.POINTER(AdamParams), cint]
     lib.situ_adam_update_host.restype = cint
     lib.situ_adam_stream_step.argtypes = [vp, vp, vp, vp, vp, i64, ctypes.POINTER(AdamParams), vp, i64, cint, cint,
@@ -352,6 +354,20 @@ def situ_glu_fwd_gateup(h, w_gate_up, expert_offsets, x=None, out=None, status=N
     return x, out
 
 
+def selftest_wait_timeout(status, elapsed_ns=None, stream=None):
+    """Launch the failure-path self-test: one CTA waits on an mbarrier nothing completes, with the
+    pipelines' bounded wait; after ~2 s it writes 1 to ``status`` (int32 [1], device, zeroed by
+    the caller) and ``elapsed_ns`` (int64 [1], device) receives the wait's duration."""
+    import torch
+    _need(status, torch.int32, (1,), "status")
+    eptr = 0
+    if elapsed_ns is not None:
+        _need(elapsed_ns, torch.int64, (1,), "elapsed_ns")
+        eptr = elapsed_ns.data_ptr()
+    with torch.cuda.device(status.device):
+        _check(load().situ_glu_selftest_wait_timeout(status.data_ptr(), eptr, _stream_handle(stream, status.device)))
+
+
 def _host_ptr(t, dtype, n, name):
     """Pointer of a contiguous CPU tensor or numpy array of `n` elements of `dtype` (torch dtype)."""
     import numpy as np
@@ -408,6 +424,6 @@ __all__ = [
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
     "situ_glu_bwd_router_dgrad", "situ_glu_fwd_gateup",
-    "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
+    "selftest_wait_timeout", "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
     "LIB_PATH", "INCLUDE",
 ]

@@ -22,9 +22,9 @@
 //                        that free ring stages ("empty") and hand accumulators to the epilogue
 //                        ("tfull"); the epilogue hands them back through "tempty";
 //   warps 2 ..           the kernel's epilogue.
-// Every wait is bounded (WAIT_LIMIT polls): on a timeout the CTA sets its abort flag and the
-// caller's status word, stops issuing work, waits (bounded) for what it already issued, frees
-// its TMEM and returns.
+// Every wait is bounded (2 s by %globaltimer, or WAIT_LIMIT polls): on a timeout the CTA sets its
+// abort flag and the caller's status word, stops issuing work, waits (bounded) for what it
+// already issued, frees its TMEM and returns.
 #pragma once
 
 #include <cuda.h>
@@ -45,7 +45,8 @@ constexpr int B_BYTES = BN * BK * 2;         // 32 KB
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
 constexpr int TMEM_COLS = 512;               // 2 accumulators x 256 columns
 constexpr int MAX_EXPERTS = 1024;           // the per-CTA tile prefix lives in shared memory
-constexpr uint32_t WAIT_LIMIT = 1u << 22;    // polls of a try_wait before giving up (~1-2 s)
+constexpr uint64_t WAIT_NS = 2000000000ull;  // a pipeline wait gives up after 2 s (%globaltimer)
+constexpr uint32_t WAIT_LIMIT = 1u << 24;    // and in any case after this many polls
 
 struct alignas(8) Barriers {
     uint64_t full[STAGES];
@@ -102,11 +103,23 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* b, uint32_t parity) {
     return ok != 0;
 }
 
-// Bounded wait; on a timeout sets the CTA's abort flag and the caller's status word.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Bounded wait; on a timeout (WAIT_NS, or WAIT_LIMIT polls) sets the CTA's abort flag and the
+// caller's status word. Returns early, false, once another role of the CTA has aborted.
 __device__ __forceinline__ bool mbar_wait(uint64_t* b, uint32_t parity, Barriers* bars, int* status) {
+    if (mbar_try_wait(b, parity)) return true;
+    const uint64_t t0 = global_ns();
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         if (mbar_try_wait(b, parity)) return true;
-        if (i > 64 && *(volatile int*)&bars->abort) return false;
+        if ((i & 63) == 63) {
+            if (*(volatile int*)&bars->abort) return false;
+            if (global_ns() - t0 > WAIT_NS) break;
+        }
     }
     *(volatile int*)&bars->abort = 1;
     if (status) atomicExch(status, 1);
@@ -275,9 +288,21 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
+// Bounded wait for the completion of work this CTA already issued (its own loads and MMAs), at the
+// end of a run or after an abort: no status, since that work completes by itself.
+__device__ __forceinline__ void mbar_drain(uint64_t* b, uint32_t parity) {
+    if (mbar_try_wait(b, parity)) return;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+        if (mbar_try_wait(b, parity)) return;
+        if ((i & 63) == 63 && global_ns() - t0 > WAIT_NS) return;
+    }
+}
+
 // Bounded wait with acquire at cluster scope (data written by other CTAs of the cluster before
 // their arrive is visible afterwards); on a timeout sets the abort flag and the status word.
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, Barriers* bars, int* status) {
+    uint64_t t0 = 0;
     for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
         uint32_t ok;
         asm volatile(
@@ -287,7 +312,11 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, 
             : "r"(smem_addr(b)), "r"(parity)
             : "memory");
         if (ok) return true;
-        if (i > 64 && *(volatile int*)&bars->abort) return false;
+        if (i == 0) t0 = global_ns();
+        if ((i & 63) == 63) {
+            if (*(volatile int*)&bars->abort) return false;
+            if (global_ns() - t0 > WAIT_NS) break;
+        }
     }
     *(volatile int*)&bars->abort = 1;
     if (status) atomicExch(status, 1);
@@ -421,9 +450,7 @@ __device__ __forceinline__ void run_producer(const Smem& sm, const Sched& sc, co
     // every load issued must land before the CTA exits: wait for each stage's last phase
     for (int s2 = 0; s2 < STAGES; ++s2) {
         if (!(pending & (1u << s2))) continue;
-        const uint32_t par = (pend_par >> s2) & 1u;
-        for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-            if (mbar_try_wait(&bars->full[s2], par)) break;
+        mbar_drain(&bars->full[s2], (pend_par >> s2) & 1u);
     }
 }
 
@@ -460,8 +487,7 @@ __device__ __forceinline__ void run_mma(const Smem& sm, const Sched& sc, uint32_
     }
     // all MMAs issued by this thread complete before TMEM is freed
     tc_commit(&bars->mma_done);
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i)
-        if (mbar_try_wait(&bars->mma_done, 0)) break;
+    mbar_drain(&bars->mma_done, 0);
 }
 
 // All threads, at the end: TMEM is freed by warp 1 once every role has finished with it.

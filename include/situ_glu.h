@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 3
+#define SITU_GLU_VERSION_MINOR 4
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -267,6 +267,13 @@ int situ_adam_update_host(float* master, void* m, void* v, const float* g, void*
 int situ_adam_stream_step(const float* grad_dev, void* weight_dev, float* master, void* m, void* v,
                           int64_t n, const situ_adam_params* hp, void* staging, int64_t chunk,
                           int nslots, int nthreads, cudaStream_t stream);
+
+/* Self-test of the tensor-core kernels' failure path (faults nothing): launches one CTA that
+ * waits, with the same bounded wait as the GEMM pipelines, on an mbarrier nothing completes. The
+ * wait gives up after about 2 s and the kernel writes 1 to *status (device int, zeroed by the
+ * caller) and returns normally; *elapsed_ns (device, may be NULL) receives how long it waited.
+ * Asynchronous on `stream`. */
+int situ_glu_selftest_wait_timeout(int* status, unsigned long long* elapsed_ns, cudaStream_t stream);
 
 /* Static, NUL-terminated description of a status code (unknown codes included). */
 const char* situ_glu_status_string(int status);

@@ -75,3 +75,35 @@ def test_stream_step_orders_after_queued_work(sg):
                              np.full(n, 0.5, np.float32), oracle.adam_hp(step=1))
     assert np.array_equal(master.view(np.uint32), ref[0].view(np.uint32))
     torch.cuda.cudart().cudaHostUnregister(staging.data_ptr())
+
+
+@pytest.mark.slow
+def test_stream_step_bench_configuration_sampled(sg):
+    """The configuration bench.py times: 2^28 parameters, chunks of 2^24, 2 slots, two chained
+    steps; checked bit for bit on 2^20 sampled parameters plus every chunk boundary (the update
+    is elementwise, so the oracle on the sample is the oracle of the whole)."""
+    n, chunk, nslots = 1 << 28, 1 << 24, 2
+    gen = torch.Generator(device=DEV).manual_seed(21)
+    master = (torch.randn(n, generator=gen, device=DEV) * 0.02).cpu().numpy()
+    m = (torch.randn(n, generator=gen, device=DEV) * 1e-3).to(torch.bfloat16).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    v = (torch.rand(n, generator=gen, device=DEV) * 1e-5).to(torch.bfloat16).cpu().view(torch.int16).numpy().view(np.uint16).copy()
+    rng = np.random.default_rng(22)
+    edges = np.concatenate([np.arange(0, n, chunk), np.arange(chunk - 1, n, chunk), [n - 1]])
+    idx = np.unique(np.concatenate([rng.integers(0, n, 1 << 20), edges]))
+    ref = (master[idx].copy(), m[idx].copy(), v[idx].copy())
+    staging = pinned(sg.adam_staging_bytes(chunk, nslots))
+    weight = torch.zeros(n, dtype=torch.bfloat16, device=DEV)
+    for step in (1, 2):
+        g = grads(n, seed=100 + step)
+        sg.situ_adam_stream_step(g, weight, master, m, v, sg.adam_params(step=step), staging, chunk, nslots)
+        torch.cuda.synchronize()
+        gi = g[torch.from_numpy(idx).to(DEV)].cpu().numpy()
+        rm, rmb, rvb, rw = oracle.adam_stored(*ref, gi, oracle.adam_hp(step=step))
+        assert np.array_equal(master[idx].view(np.uint32), rm.view(np.uint32))
+        assert np.array_equal(m[idx], rmb) and np.array_equal(v[idx], rvb)
+        wi = weight[torch.from_numpy(idx).to(DEV)].cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(wi, rw)
+        ref = (rm, rmb, rvb)
+    torch.cuda.cudart().cudaHostUnregister(staging.data_ptr())
+    del weight
+    torch.cuda.empty_cache()

@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10300
+    assert sg.version() == 10400
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
@@ -232,3 +232,9 @@ def test_gateup_validates_before_any_launch(lib):
     assert gateup(lib, h, w, off, E, x, x + 1024, st, R, H, D) == OVERLAP      # out inside x
     assert gateup(lib, h, w, off, E, x, off - 32, st, R, H, D) == OVERLAP      # out over offsets
     assert gateup(lib, h, w, off, E, x, out, out + 8, R, H, D) == OVERLAP      # status inside out
+
+
+def test_selftest_validates(lib):
+    assert lib.situ_glu_selftest_wait_timeout(None, None, None) == INVALID
+    assert lib.situ_glu_selftest_wait_timeout(A + 2, None, None) == INVALID        # status needs 4 bytes
+    assert lib.situ_glu_selftest_wait_timeout(A, A + 4, None) == INVALID           # elapsed needs 8 bytes
