@@ -12,10 +12,11 @@
 // The GEMM pipeline (persistent CTAs over 128-row M-tiles of one expert, TMA producer warp,
 // single-thread tcgen05.mma issuer, two TMEM accumulators, bounded mbarrier waits) is the one in
 // situ_tc.cuh, with A = dY and B = W_downᵀ (rows e·H + nt·256 ..). The epilogue here:
-//   EPW warps per 32-lane TMEM quadrant, each with a slice of the 256 columns of a job; a thread
-//   owns one row, reads its g with tcgen05.ld, loads the matching x (prefetched one chunk ahead,
-//   32-byte loads), and writes dx; its dp partial stays in a register across the N-tiles of the
-//   row and the EPW partials of a row are summed through shared memory at the end of the M-tile.
+//   EPW = 3 warps per 32-lane TMEM quadrant (12 warps: 3 per SM sub-partition, 128 registers),
+//   taking a job's 16-column chunks in turn; a thread owns one row, reads its g with tcgen05.ld,
+//   loads the matching x (prefetched one chunk ahead, 32-byte loads), and writes dx; its dp
+//   partial stays in a register across the N-tiles of the row and the EPW partials of a row are
+//   summed through shared memory at the end of the M-tile.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <math.h>
@@ -33,14 +34,21 @@ using namespace situ;
 using namespace situ_host;
 using namespace situ_tc;
 
-constexpr int EPW = 2;                       // epilogue warps per 32-lane TMEM quadrant
-constexpr int CW = 32;                       // accumulator columns per tcgen05.ld chunk
+constexpr int EPW = 3;                       // epilogue warps per 32-lane TMEM quadrant
+constexpr int CW = 16;                       // accumulator columns per tcgen05.ld chunk
 constexpr int NUM_EPI_THREADS = 4 * EPW * 32;
 constexpr int NUM_THREADS = 64 + NUM_EPI_THREADS;  // warp 0 TMA, warp 1 MMA, then the epilogue
-constexpr int COLS_PER_WARP = BN / EPW;      // accumulator columns of one job an epilogue warp owns
-constexpr int CPJ = COLS_PER_WARP / CW;      // chunks per job per epilogue warp
+constexpr int NCH = BN / CW;                 // chunks of a job; warp slot s takes chunks s, s + EPW, ...
+constexpr int MAXC = (NCH + EPW - 1) / EPW;  // chunks of a job for the busiest slot
+constexpr int NBUF = 3;                      // x register buffers, rotating; a job's first chunk uses 0
 constexpr int XV = CW / 16;                  // 32-byte vectors (16 bf16) per half-row per chunk
-static_assert(CPJ >= 2 && CPJ % 2 == 0, "the x prefetch alternates two register buffers");
+static_assert(XV == 1, "one 32-byte vector per half-row per chunk");
+constexpr bool buffers_ok() {                // a slot's last chunk of a job never uses buffer 0,
+    for (int s = 0; s < EPW; ++s)            // which the prefetch of the next job's first chunk fills
+        if (((NCH - s + EPW - 1) / EPW - 1) % NBUF == 0) return false;
+    return true;
+}
+static_assert(buffers_ok(), "x buffer rotation across job boundaries");
 constexpr int DGRAD_SPLIT = 4;               // CTAs per cluster sharing an M-tile (each every 4th N-tile)
 constexpr int MAX_SPLIT = DGRAD_SPLIT;
 // extra shared memory: dp_part [EPW][BM] | dp_cl [2][MAX_SPLIT][BM] | dp_full[2], dp_free[2]
@@ -93,11 +101,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) run_mma(sm, sc, tmem, T, NT, KB, status);
     } else {
         // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
-        // A warp may read only the TMEM lanes of quadrant warp % 4; the EPW warps of a quadrant split
-        // each job's 256 columns into EPW slices of COLS_PER_WARP, read CW columns at a time. One
-        // thread owns one row for a whole M-tile: its x is fetched with 32-byte loads one chunk ahead
-        // (across job boundaries too, as x does not depend on the accumulator), so the loads are in
-        // flight while the previous chunk is computed and while the next accumulator is awaited.
+        // A warp may read only the TMEM lanes of quadrant warp % 4; the EPW warps of a quadrant take
+        // a job's 16-column chunks in turn (slot s: chunks s, s + EPW, ...). One thread owns one row
+        // for a whole M-tile: the x of its next chunk is fetched with 32-byte loads before the
+        // current chunk is computed (also across job boundaries, as x does not depend on the
+        // accumulator), so the loads are in flight while the previous chunk is computed and while
+        // the next accumulator is awaited.
         const int quad = warp & 3;
         const int slot = (warp - 2) >> 2;
         const int lrow = quad * 32 + lane;         // row within the tile
@@ -111,17 +120,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t row = row0 + lrow;
             const bool valid = ok && row >= 0 && row < row_end;
             const float pr16 = valid ? 16.0f * p[row] : 0.0f;
-            const uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * COLS_PER_WARP;
-            uint16_t* dxr = dx + (valid ? row : 0) * 2 * H + slot * COLS_PER_WARP;
+            const uint16_t* xr = x + (valid ? row : 0) * 2 * H;
+            uint16_t* dxr = dx + (valid ? row : 0) * 2 * H;
             float acc_dp = 0.0f;
-            Vec<8> xb[2][2][XV];                   // [buffer][gate, linear][32-byte vector]
-            if (valid) {                           // first chunk: (first N-tile of this CTA, 0)
-                const int64_t j1 = (int64_t)sc.n0 * BN;
-#pragma unroll
-                for (int v = 0; v < XV; ++v) {
-                    xb[0][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + j1 + 16 * v));
-                    xb[0][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + j1 + 16 * v));
-                }
+            Vec<8> xb[NBUF][2];                    // [buffer][gate, linear]
+            if (valid) {                           // first chunk: (first N-tile of this CTA, chunk slot)
+                const int64_t j1 = (int64_t)sc.n0 * BN + slot * CW;
+                xb[0][0] = ld_stream<8, true>((const Vec<8>*)(xr + j1));
+                xb[0][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + j1));
             }
             for (int nt = sc.n0; nt < NT; nt += sc.nstep, ++job) {
                 const int acc = job & 1;
@@ -130,42 +136,45 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ok = __all_sync(0xffffffffu, ok);                 // tcgen05.ld below is warp-collective
                 tc_fence_after();
 #pragma unroll
-                for (int k = 0; k < CPJ; ++k) {
-                    const int cur = k & 1;
-                    // prefetch the next chunk of this row: (nt, k + 1), or (next N-tile, 0) after the last
-                    const bool last = (k + 1 == CPJ);
-                    if (valid && (!last || nt + sc.nstep < NT)) {
-                        const int64_t jn = last ? (int64_t)(nt + sc.nstep) * BN : (int64_t)nt * BN + (k + 1) * CW;
-#pragma unroll
-                        for (int v = 0; v < XV; ++v) {
-                            xb[cur ^ 1][0][v] = ld_stream<8, true>((const Vec<8>*)(xr + jn + 16 * v));
-                            xb[cur ^ 1][1][v] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn + 16 * v));
+                for (int i = 0; i < MAXC; ++i) {
+                    const int kk = slot + i * EPW;                // this warp's i-th chunk of the job
+                    if (kk < NCH) {
+                        const int cur = i % NBUF;
+                        const bool last = kk + EPW >= NCH;        // this warp's last chunk of the job
+                        // prefetch the next chunk: (nt, kk + EPW), or (next N-tile, slot) after the last
+                        if (last) {
+                            if (valid && nt + sc.nstep < NT) {
+                                const int64_t jn = (int64_t)(nt + sc.nstep) * BN + slot * CW;
+                                xb[0][0] = ld_stream<8, true>((const Vec<8>*)(xr + jn));
+                                xb[0][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn));
+                            }
+                        } else if (valid) {
+                            const int64_t jn = (int64_t)nt * BN + (kk + EPW) * CW;
+                            xb[(i + 1) % NBUF][0] = ld_stream<8, true>((const Vec<8>*)(xr + jn));
+                            xb[(i + 1) % NBUF][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn));
                         }
-                    }
-                    float gv[CW];
-                    if (ok) tc_ld<CW>(tmem + t_lane + (uint32_t)(acc * BN + slot * COLS_PER_WARP + k * CW), gv);
-                    if (last) {
-                        tc_fence_before();
-                        mbar_arrive(&bars->tempty[acc]);       // accumulator may be overwritten
-                    }
-                    if (ok && valid) {
-                        const int64_t j0 = (int64_t)nt * BN + k * CW;
-#pragma unroll
-                        for (int v = 0; v < XV; ++v) {
+                        float gv[CW];
+                        if (ok) tc_ld<CW>(tmem + t_lane + (uint32_t)(acc * BN + kk * CW), gv);
+                        if (last) {
+                            tc_fence_before();
+                            mbar_arrive(&bars->tempty[acc]);     // accumulator may be overwritten
+                        }
+                        if (ok && valid) {
+                            const int64_t j0 = (int64_t)nt * BN + kk * CW;
                             Vec<8> dgo, dlo;
 #pragma unroll
-                            for (int i = 0; i < 8; ++i) {
-                                const uint32_t gw = xb[cur][0][v].w[i], lw = xb[cur][1][v].w[i];
-                                const float g0 = gv[16 * v + 2 * i], g1 = gv[16 * v + 2 * i + 1];
+                            for (int q = 0; q < 8; ++q) {
+                                const uint32_t gw = xb[cur][0].w[q], lw = xb[cur][1].w[q];
+                                const float g0 = gv[2 * q], g1 = gv[2 * q + 1];
                                 situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gw), bf16_lo(lw), pr16 * g0, c);
                                 situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gw), bf16_hi(lw), pr16 * g1, c);
                                 acc_dp = fmaf(g0, b0.a16, acc_dp);
                                 acc_dp = fmaf(g1, b1.a16, acc_dp);
-                                dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
-                                dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
+                                dgo.w[q] = pack_bf16x2(b0.dgate, b1.dgate);
+                                dlo.w[q] = pack_bf16x2(b0.dlin, b1.dlin);
                             }
-                            st_stream<8>((Vec<8>*)(dxr + j0 + 16 * v), dgo);
-                            st_stream<8>((Vec<8>*)(dxr + H + j0 + 16 * v), dlo);
+                            st_stream<8>((Vec<8>*)(dxr + j0), dgo);
+                            st_stream<8>((Vec<8>*)(dxr + H + j0), dlo);
                         }
                     }
                 }
