@@ -780,13 +780,42 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_ro
     torch.cuda.synchronize(dev)
     barrier(world)
     ms = max_over_ranks(start.elapsed_time(end), world, dev)
+
+    # the host link of this machine, measured on the same buffers: x alone each way, then both
+    # directions at once (x in, dx out on two streams) — the step cannot beat moving its bytes
+    def copy_ms(fn, reps=3):
+        fn()
+        torch.cuda.synchronize(dev)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize(dev)
+        return e0.elapsed_time(e1) / reps
+
+    def both_ways():
+        with torch.cuda.stream(s_in):
+            x.copy_(xh, non_blocking=True)
+        with torch.cuda.stream(s_out):
+            dxh.copy_(dx, non_blocking=True)
+        torch.cuda.current_stream(dev).wait_stream(s_in)
+        torch.cuda.current_stream(dev).wait_stream(s_out)
+    nbx = xh.numel() * 2
+    t_in = copy_ms(lambda: x.copy_(xh, non_blocking=True))
+    t_out = copy_ms(lambda: dxh.copy_(dx, non_blocking=True))
+    t_both = copy_ms(both_ways)
+    link = {"h2d_GB_s": nbx / t_in / 1e6, "d2h_GB_s": nbx / t_out / 1e6, "both_ways_GB_s": 2 * nbx / t_both / 1e6}
+    link_ms = (h2d + d2h) / (link["both_ways_GB_s"] * 1e6)
     for t in (xh, gh, ph, oh, dxh, dph):
         unpin(t)
     return {"value": whole_job_rate(R, world, steps, ms * 1e-3), "unit": "rows/s", "steps": steps,
             "ms_per_step": ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "gpu_launches": launches[0],
+            "host_link": link, "link_bound_ms_per_step": link_ms, "frac_of_link_bound": link_ms / (ms / steps),
             "how": f"page-locked host x,g,p -> device -> fwd + bwd via the binding -> out,dx,dp -> host, "
-                   f"streamed over {n} row chunks of {chunk_rows} on 3 CUDA streams"}
+                   f"streamed over {n} row chunks of {chunk_rows} on 3 CUDA streams; host_link measured on "
+                   f"the same buffers in the same run"}
 
 
 def main(argv=None):
