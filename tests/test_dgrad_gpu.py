@@ -133,3 +133,47 @@ def test_dgrad_expert_grouped_full_size_sampled(sg):
     par.assert_ok()
     del x, dy, wt, dx, dp
     torch.cuda.empty_cache()
+
+
+def test_dgrad_max_experts_mostly_empty(sg):
+    """1024 experts (the per-launch maximum; the whole M-tile prefix in shared memory), 600 rows
+    spread over 37 of them, the rest empty; on a non-default stream."""
+    rng = np.random.default_rng(8)
+    counts = np.zeros(1024, dtype=np.int64)
+    used = rng.choice(1024, 37, replace=False)
+    counts[used] = rng.multinomial(600, np.ones(37) / 37)
+    counts[1023] += 1                                   # the last expert owns the last row
+    x, dy, wt, off, p = make(counts.tolist(), 256, 64, seed=17, x_std=2.0)
+    s = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with torch.cuda.stream(s):
+        dx, dp = sg.situ_glu_bwd_router_dgrad(x.to(DEV), dy.to(DEV), wt.to(DEV), off.to(DEV), p.to(DEV),
+                                              status=status, stream=s)
+    s.synchronize()
+    assert int(status.item()) == 0
+    dx_ref, dp_ref, dpa = oracle.dgrad_bwd_router(bits_of(x), bits_of(dy), bits_of(wt).reshape(wt.shape),
+                                                 off.numpy(), p.numpy())
+    par = Parity("dgrad 1024 experts")
+    par.bf16("dx", bits_of(dx), dx_ref)
+    par.dp(dp.cpu().numpy(), dp_ref, dpa)
+    par.assert_ok()
+
+
+def test_dgrad_single_row(sg):
+    x, dy, wt, off, p = make([0, 1, 0], 512, 128, seed=18)
+    dx, dp = run(sg, x, dy, wt, off, p)
+    dx_ref, dp_ref, dpa = oracle.dgrad_bwd_router(bits_of(x), bits_of(dy), bits_of(wt).reshape(wt.shape),
+                                                 off.numpy(), p.numpy())
+    par = Parity("dgrad single row")
+    par.bf16("dx", bits_of(dx), dx_ref)
+    par.dp(dp.cpu().numpy(), dp_ref, dpa)
+    par.assert_ok()
+
+
+def test_dgrad_rejects_too_many_experts(sg):
+    x, dy, wt, off, p = make([1] * 2, 256, 64, seed=19)
+    big = torch.zeros(1025, 256, 64, dtype=torch.bfloat16, device=DEV)
+    offs = torch.zeros(1026, dtype=torch.int64, device=DEV)
+    offs[-1] = 2
+    with pytest.raises(sg.SituGluError):
+        sg.situ_glu_bwd_router_dgrad(x.to(DEV), dy.to(DEV), big, offs, p.to(DEV))

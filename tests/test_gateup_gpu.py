@@ -163,3 +163,27 @@ def test_gateup_expert_grouped_full_size_sampled(sg):
     assert differs <= max(8, xg.size // 200)
     del h, w, x, out
     torch.cuda.empty_cache()
+
+
+def test_gateup_max_experts_mostly_empty(sg):
+    """1024 experts, 600 rows over 37 of them, on a non-default stream."""
+    rng = np.random.default_rng(9)
+    counts = np.zeros(1024, dtype=np.int64)
+    used = rng.choice(1024, 37, replace=False)
+    counts[used] = rng.multinomial(600, np.ones(37) / 37)
+    h, w, off = make(counts.tolist(), 128, 64, seed=23)
+    s = torch.cuda.Stream()
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    with torch.cuda.stream(s):
+        x, out = sg.situ_glu_fwd_gateup(h.to(DEV), w.to(DEV), off.to(DEV), status=status, stream=s)
+    s.synchronize()
+    assert int(status.item()) == 0
+    x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy())
+    check("gateup 1024 experts", bits_of(x), bits_of(out), x_exact, xb_ref, mag)
+
+
+def test_gateup_single_row(sg):
+    h, w, off = make([0, 0, 1], 256, 64, seed=24)
+    x, out = run(sg, h, w, off)
+    x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy())
+    check("gateup single row", bits_of(x), bits_of(out), x_exact, xb_ref, mag)
