@@ -236,6 +236,47 @@ def fp8_scale_blocks(H: int) -> int:
     return -(-H // FP8_BLOCK)
 
 
+_SituAndMul = None
+
+
+def _situ_and_mul_fn():
+    """The autograd Function, created on first use (torch is imported lazily by this module)."""
+    global _SituAndMul
+    if _SituAndMul is None:
+        import torch
+
+        class SituAndMul(torch.autograd.Function):
+            """SiTU-GLU as an autograd operator that keeps only the bf16 input for the backward
+            ("Frontier-scale RL with Kimi K3", section "Streaming activations": the custom
+            operator drops every tensor but x and recomputes tanh and sigmoid). Forward: the
+            forward kernel. Backward: the fused backward kernel with a unit router weight, so
+            dL/dx = dL/da · da/dx (its router gradient, <dL/da, a>, is not needed here)."""
+
+            @staticmethod
+            def forward(ctx, x, beta, lbeta):
+                ctx.save_for_backward(x)
+                ctx.beta, ctx.lbeta = beta, lbeta
+                return situ_glu_fwd(x, beta=beta, lbeta=lbeta)
+
+            @staticmethod
+            def backward(ctx, grad_out):
+                (x,) = ctx.saved_tensors
+                g = grad_out.contiguous()
+                ones = torch.ones(x.shape[0], dtype=torch.float32, device=x.device)
+                dx, _ = situ_glu_bwd_router(x, g, ones, beta=ctx.beta, lbeta=ctx.lbeta)
+                return dx, None, None
+
+        _SituAndMul = SituAndMul
+    return _SituAndMul
+
+
+def situ_and_mul(x, beta: float = 4.0, linear_beta: float = 25.0):
+    """a = beta·tanh(gate/beta)·sigmoid(gate) · linear_beta·tanh(linear/linear_beta) for
+    x = [gate | linear] (bf16 [R, 2H] on the GPU), differentiable; only x is kept for the
+    backward. The same interface as the pages' custom operator, on this library's kernels."""
+    return _situ_and_mul_fn().apply(x, float(beta), float(linear_beta))
+
+
 def situ_glu_fwd_save_fp8(x, out=None, xq=None, xs=None, beta: float = 4.0, lbeta: float = 25.0, stream=None):
     """(out bf16 [R,H], xq uint8 [R,2H], xs fp32 [R,2*nb]): the forward plus x saved in block-wise FP8."""
     import torch
@@ -424,6 +465,6 @@ __all__ = [
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
     "situ_glu_bwd_router_dgrad", "situ_glu_fwd_gateup",
-    "selftest_wait_timeout", "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
+    "situ_and_mul", "selftest_wait_timeout", "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
     "LIB_PATH", "INCLUDE",
 ]

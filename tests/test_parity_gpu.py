@@ -480,3 +480,23 @@ def test_small_magnitude_rows(sg, scale):
     par8 = Parity(f"fp8, small magnitude x ~ N(0, {scale}^2)")
     check_fp8_full(par8, x, g, p, out8, xq, xs, dx8, dp8)
     par8.assert_ok()
+
+
+def test_situ_and_mul_autograd(sg):
+    """The autograd operator: forward equals the oracle's, the gradient it passes back equals the
+    oracle's backward at p = 1 with the incoming gradient as g, and it saves only x."""
+    gen = torch.Generator().manual_seed(41)
+    x = (torch.randn(300, 2 * 1024, generator=gen) * 3).to(torch.bfloat16).to(DEV).requires_grad_(True)
+    g = torch.randn(300, 1024, generator=gen).to(torch.bfloat16).to(DEV)
+    saved = []
+    with torch.autograd.graph.saved_tensors_hooks(lambda t: saved.append(t) or t, lambda t: t):
+        a = sg.situ_and_mul(x)
+    a.backward(g)
+    torch.cuda.synchronize()
+    assert len(saved) == 1 and saved[0].data_ptr() == x.data_ptr()
+    xb, gb = bits_of(x.detach()), bits_of(g)
+    par = Parity("situ_and_mul autograd")
+    par.bf16("out", bits_of(a.detach()), oracle.fwd_bf16(xb))
+    dx_ref, _, _ = oracle.bwd_router_bf16(xb, gb, np.ones(300, dtype=np.float32))
+    par.bf16("dx", bits_of(x.grad), dx_ref)
+    par.assert_ok()
