@@ -10,9 +10,11 @@
 // same bf16 x, so the result equals the unfused projection followed by situ_glu_fwd, with one
 // fewer round trip of x through memory.
 //
-// The GEMM pipeline is the one in situ_tc.cuh with A = h and a B tile made of two 128-row
-// halves: rows nt·128 .. of W_gate,e and the same rows of W_up,e, so accumulator column c < 128
-// holds gate column nt·128 + c and column 128 + c the matching linear column. Epilogue: EPW warps
+// The GEMM pipeline is the one in situ_tc.cuh — for experts of many rows its two-M-tile form, in
+// which two M-tiles of one expert share every weight stage (chosen per launch from the mean rows
+// per expert) — with A = h and a B tile made of two 128-row halves: rows nt·128 .. of W_gate,e
+// and the same rows of W_up,e, so accumulator column c < 128 holds gate column nt·128 + c and
+// column 128 + c the matching linear column. Epilogue: EPW warps
 // per 32-lane TMEM quadrant, each owning 128/EPW of a job's 128 column pairs; a thread owns one
 // row, reads 32 gate and 32 linear accumulators per chunk, rounds them to bf16 (nearest even),
 // evaluates the forward on the rounded values and writes x (both halves) and out with 32-byte
@@ -48,7 +50,12 @@ constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 128 + STAGE_BYTES_EPI;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 constexpr int CSPLIT = 8;                    // CTAs sharing an M-tile (each every 8th N-tile)
 
-template <bool BETA4>
+// UNIT = M-tiles per work unit: 1 (two double-buffered accumulators, the next job's MMAs overlap
+// this job's epilogue) or 2 (two M-tiles share every weight stage, a third fewer bytes per MMA
+// flop, no overlap). The host picks 2 when experts average at least UNIT2_MIN_ROWS rows.
+constexpr int64_t UNIT2_MIN_ROWS = 4 * BM;
+
+template <bool BETA4, int UNIT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gateup_fwd_kernel(const __grid_constant__ CUtensorMap map_h, const __grid_constant__ CUtensorMap map_w,
                       const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_out,
@@ -62,20 +69,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const Sched sc = make_sched(csplit);
     uint32_t tmem;
-    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem);
+    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem, UNIT);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer: B = W_gate,e and W_up,e rows nt·128 ..
-        if (lane == 0)
-            run_producer(sm, sc, &map_h, offsets, E, R, T, NT, KB, status,
-                         [&](uint8_t* sb, int e, int nt, int kb, uint64_t* bar, uint64_t pol) {
-                             const int64_t r0 = (int64_t)e * 2 * H + (int64_t)nt * HN;
-                             tma_load_2d_hint(sb, &map_w, kb * BK, (int)r0, bar, pol);
-                             tma_load_2d_hint(sb + HN * BK * 2, &map_w, kb * BK, (int)(r0 + H), bar, pol);
-                         });
+        auto load_b = [&](uint8_t* sb, int e, int nt, int kb, uint64_t* bar, uint64_t pol) {
+            const int64_t r0 = (int64_t)e * 2 * H + (int64_t)nt * HN;
+            tma_load_2d_hint(sb, &map_w, kb * BK, (int)r0, bar, pol);
+            tma_load_2d_hint(sb + HN * BK * 2, &map_w, kb * BK, (int)(r0 + H), bar, pol);
+        };
+        if (lane == 0) {
+            if constexpr (UNIT == 2)
+                run_producer2(sm, sc, &map_h, offsets, E, R, T, NT, KB, status, load_b);
+            else
+                run_producer(sm, sc, &map_h, offsets, E, R, T, NT, KB, status, load_b);
+        }
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) run_mma(sm, sc, tmem, T, NT, KB, status);
+        if (lane == 0) {
+            if constexpr (UNIT == 2)
+                run_mma2(sm, sc, tmem, offsets, E, R, T, NT, KB, status);
+            else
+                run_mma(sm, sc, tmem, T, NT, KB, status);
+        }
     } else {
         // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
         const int quad = warp & 3;
@@ -89,77 +105,85 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool stores_pending = false;                            // lane 0 has TMA stores in flight
         int job = 0;
         bool ok = true;
-        for (int t = sc.t0; t < T; t += sc.tstep) {
-            int e;
-            int64_t row0, row_end;
-            tile_rows(sm.tile_start, offsets, E, R, t, e, row0, row_end);
-            const int64_t row = row0 + lrow;
-            const bool valid = ok && row >= 0 && row < row_end;
-            // all 32 rows of this warp's quadrant belong to the expert: x and out leave through TMA stores
-            const bool full_quad = row0 + quad * 32 + 31 < row_end;
-            uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * PAIRS_PER_WARP;
-            uint16_t* outr = out + (valid ? row : 0) * H + slot * PAIRS_PER_WARP;
+        for (int u = sc.t0; u < T; u += sc.tstep) {
+            int e, ntiles = 1;
+            int64_t urow0, row_end;
+            if constexpr (UNIT == 2)
+                unit2_rows(sm.tile_start, offsets, E, R, u, e, urow0, row_end, ntiles);
+            else
+                tile_rows(sm.tile_start, offsets, E, R, u, e, urow0, row_end);
             for (int nt = sc.n0; nt < NT; nt += sc.nstep, ++job) {
-                const int acc = job & 1;
-                const uint32_t acc_phase = (uint32_t)((job >> 1) & 1);
-                if (ok && !mbar_wait(&bars->tfull[acc], acc_phase, bars, status)) ok = false;
+                // UNIT 1: accumulator job & 1 through barrier pair job & 1; UNIT 2: both, through pair 0
+                const int bi = UNIT == 2 ? 0 : (job & 1);
+                const uint32_t par = UNIT == 2 ? (uint32_t)(job & 1) : (uint32_t)((job >> 1) & 1);
+                if (ok && !mbar_wait(&bars->tfull[bi], par, bars, status)) ok = false;
                 ok = __all_sync(0xffffffffu, ok);                 // tcgen05.ld below is warp-collective
                 tc_fence_after();
+                for (int m = 0; m < ntiles; ++m) {               // the unit's M-tiles
+                    const int acc_col = UNIT == 2 ? m * BN : bi * BN;
+                    const int64_t row0 = urow0 + (int64_t)m * BM;
+                    const int64_t row = row0 + lrow;
+                    const bool valid = ok && row >= 0 && row < row_end;
+                    // all 32 rows of this warp's quadrant belong to the expert: x and out leave through TMA stores
+                    const bool full_quad = row0 + quad * 32 + 31 < row_end;
+                    uint16_t* xr = x + (valid ? row : 0) * 2 * H + slot * PAIRS_PER_WARP;
+                    uint16_t* outr = out + (valid ? row : 0) * H + slot * PAIRS_PER_WARP;
 #pragma unroll
-                for (int k = 0; k < CPJ; ++k) {
-                    uint32_t gr[CW], lr[CW];
-                    if (ok) {
-                        const uint32_t col = (uint32_t)(acc * BN + slot * PAIRS_PER_WARP + k * CW);
-                        tc_ld_issue<CW>(tmem + t_lane + col, gr);
-                        tc_ld_issue<CW>(tmem + t_lane + col + HN, lr);
-                        tc_wait_ld();
-                    }
-                    if (k + 1 == CPJ) {
-                        tc_fence_before();
-                        mbar_arrive(&bars->tempty[acc]);       // accumulator may be overwritten
-                    }
-                    static_assert(CW == 16, "one 32-byte vector per output row per chunk");
-                    Vec<8> xg, xl, o;
-                    if (ok && valid) {
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            xg.w[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
-                            xl.w[i] = pack_bf16x2(__uint_as_float(lr[2 * i]), __uint_as_float(lr[2 * i + 1]));
-                            const float a0 = situ::fwd<BETA4>(bf16_lo(xg.w[i]), bf16_lo(xl.w[i]), c);
-                            const float a1 = situ::fwd<BETA4>(bf16_hi(xg.w[i]), bf16_hi(xl.w[i]), c);
-                            o.w[i] = pack_bf16x2(a0, a1);
+                    for (int k = 0; k < CPJ; ++k) {
+                        uint32_t gr[CW], lr[CW];
+                        if (ok) {
+                            const uint32_t col = (uint32_t)(acc_col + slot * PAIRS_PER_WARP + k * CW);
+                            tc_ld_issue<CW>(tmem + t_lane + col, gr);
+                            tc_ld_issue<CW>(tmem + t_lane + col + HN, lr);
+                            tc_wait_ld();
                         }
-                    }
-                    const int64_t jl = (int64_t)nt * HN + k * CW;                        // within the slice
-                    const int64_t j0 = jl + slot * PAIRS_PER_WARP;                       // column in [0, H)
-                    if (ok && full_quad) {
-                        // the warp's 32 rows x CW columns of x (both halves) and of out: staged, then
-                        // one TMA store each
-                        if (stores_pending) {
-                            if (lane == 0) bulk_wait_read_all();     // the previous tiles have been read out
+                        if (m + 1 == ntiles && k + 1 == CPJ) {
+                            tc_fence_before();
+                            mbar_arrive(&bars->tempty[bi]);      // the job's accumulators may be overwritten
+                        }
+                        static_assert(CW == 16, "one 32-byte vector per output row per chunk");
+                        Vec<8> xg, xl, o;
+                        if (ok && valid) {
+#pragma unroll
+                            for (int i = 0; i < 8; ++i) {
+                                xg.w[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
+                                xl.w[i] = pack_bf16x2(__uint_as_float(lr[2 * i]), __uint_as_float(lr[2 * i + 1]));
+                                const float a0 = situ::fwd<BETA4>(bf16_lo(xg.w[i]), bf16_lo(xl.w[i]), c);
+                                const float a1 = situ::fwd<BETA4>(bf16_hi(xg.w[i]), bf16_hi(xl.w[i]), c);
+                                o.w[i] = pack_bf16x2(a0, a1);
+                            }
+                        }
+                        const int64_t jl = (int64_t)nt * HN + k * CW;                        // within the slice
+                        const int64_t j0 = jl + slot * PAIRS_PER_WARP;                       // column in [0, H)
+                        if (ok && full_quad) {
+                            // the warp's 32 rows x CW columns of x (both halves) and of out: staged, then
+                            // one TMA store each
+                            if (stores_pending) {
+                                if (lane == 0) bulk_wait_read_all();     // the previous tiles have been read out
+                                __syncwarp();
+                            }
+                            st_shared_v4(st_g + lane * 32, xg.w[0], xg.w[1], xg.w[2], xg.w[3]);
+                            st_shared_v4(st_g + lane * 32 + 16, xg.w[4], xg.w[5], xg.w[6], xg.w[7]);
+                            st_shared_v4(st_l + lane * 32, xl.w[0], xl.w[1], xl.w[2], xl.w[3]);
+                            st_shared_v4(st_l + lane * 32 + 16, xl.w[4], xl.w[5], xl.w[6], xl.w[7]);
+                            st_shared_v4(st_o + lane * 32, o.w[0], o.w[1], o.w[2], o.w[3]);
+                            st_shared_v4(st_o + lane * 32 + 16, o.w[4], o.w[5], o.w[6], o.w[7]);
+                            fence_proxy_async_smem();
                             __syncwarp();
+                            if (lane == 0) {
+                                const int r0q = (int)(row0 + quad * 32);
+                                tma_store_2d(&map_x, (int)j0, r0q, st_g);
+                                tma_store_2d(&map_x, (int)(H + j0), r0q, st_l);
+                                tma_store_2d(&map_out, (int)j0, r0q, st_o);
+                                bulk_commit();
+                            }
+                            stores_pending = true;
+                        } else if (ok && valid) {
+                            // a quadrant crossing the expert's end: only this row, from registers
+                            st_stream<8>((Vec<8>*)(xr + jl), xg);
+                            st_stream<8>((Vec<8>*)(xr + H + jl), xl);
+                            st_stream<8>((Vec<8>*)(outr + jl), o);
                         }
-                        st_shared_v4(st_g + lane * 32, xg.w[0], xg.w[1], xg.w[2], xg.w[3]);
-                        st_shared_v4(st_g + lane * 32 + 16, xg.w[4], xg.w[5], xg.w[6], xg.w[7]);
-                        st_shared_v4(st_l + lane * 32, xl.w[0], xl.w[1], xl.w[2], xl.w[3]);
-                        st_shared_v4(st_l + lane * 32 + 16, xl.w[4], xl.w[5], xl.w[6], xl.w[7]);
-                        st_shared_v4(st_o + lane * 32, o.w[0], o.w[1], o.w[2], o.w[3]);
-                        st_shared_v4(st_o + lane * 32 + 16, o.w[4], o.w[5], o.w[6], o.w[7]);
-                        fence_proxy_async_smem();
-                        __syncwarp();
-                        if (lane == 0) {
-                            const int r0q = (int)(row0 + quad * 32);
-                            tma_store_2d(&map_x, (int)j0, r0q, st_g);
-                            tma_store_2d(&map_x, (int)(H + j0), r0q, st_l);
-                            tma_store_2d(&map_out, (int)j0, r0q, st_o);
-                            bulk_commit();
-                        }
-                        stores_pending = true;
-                    } else if (ok && valid) {
-                        // a quadrant crossing the expert's end: only this row, from registers
-                        st_stream<8>((Vec<8>*)(xr + jl), xg);
-                        st_stream<8>((Vec<8>*)(xr + H + jl), xl);
-                        st_stream<8>((Vec<8>*)(outr + jl), o);
                     }
                 }
             }
@@ -205,7 +229,9 @@ int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* exp
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
-    auto kernel = b4 ? gateup_fwd_kernel<true> : gateup_fwd_kernel<false>;
+    const bool unit2 = R / E >= UNIT2_MIN_ROWS;
+    auto kernel = b4 ? (unit2 ? gateup_fwd_kernel<true, 2> : gateup_fwd_kernel<true, 1>)
+                     : (unit2 ? gateup_fwd_kernel<false, 2> : gateup_fwd_kernel<false, 1>);
     cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e);
     const int NT = (int)(H / HN);

@@ -358,19 +358,36 @@ __device__ __forceinline__ Sched make_sched(int csplit) {
     return s;
 }
 
+// Work unit u of two M-tiles -> (expert, first row, end row of the expert, M-tiles in the unit:
+// 2, or 1 for the last unit of an expert with an odd number of M-tiles).
+__device__ __forceinline__ void unit2_rows(const int* unit_start, const int64_t* off, int E, int64_t R, int u,
+                                           int& e, int64_t& row0, int64_t& row_end, int& ntiles) {
+    int lo = 0, hi = E - 1;                 // last e with unit_start[e] <= u
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (unit_start[mid] <= u) lo = mid; else hi = mid - 1;
+    }
+    e = lo;
+    row0 = off[e] + (int64_t)(u - unit_start[e]) * 2 * BM;
+    row_end = off[e + 1] < R ? off[e + 1] : R;
+    ntiles = row_end - row0 > BM ? 2 : 1;
+}
+
 // ---------------------------------------------------------------- pipeline phases
 
-// All threads: per-expert M-tile prefix (each CTA builds its own copy: counts in parallel, then
-// one warp scans them, each lane a contiguous segment, shuffles across lanes), barrier init, TMEM
-// allocation by warp 1. Returns the number of M-tiles; *tmem receives the TMEM base address.
+// All threads: per-expert prefix of work units of unit_tiles M-tiles each (each CTA builds its own
+// copy: counts in parallel, then one warp scans them, each lane a contiguous segment, shuffles
+// across lanes), barrier init, TMEM allocation by warp 1. Returns the number of units; *tmem
+// receives the TMEM base address.
 __device__ __forceinline__ int pipeline_setup(const Smem& sm, const int64_t* offsets, int E, int num_epi_threads,
-                                              uint32_t* tmem) {
+                                              uint32_t* tmem, int unit_tiles = 1) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Barriers* bars = sm.bars;
-    int* tile_start = sm.tile_start;
+    int* tile_start = sm.tile_start;             // per expert: its first work unit
+    const int64_t unit_rows = (int64_t)unit_tiles * BM;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
         const int64_t n = offsets[e + 1] - offsets[e];
-        tile_start[e + 1] = n > 0 ? (int)((n + BM - 1) / BM) : 0;
+        tile_start[e + 1] = n > 0 ? (int)((n + unit_rows - 1) / unit_rows) : 0;
     }
     if (threadIdx.x == 0) {
         tile_start[0] = 0;
@@ -486,6 +503,87 @@ __device__ __forceinline__ void run_mma(const Smem& sm, const Sched& sc, uint32_
         }
     }
     // all MMAs issued by this thread complete before TMEM is freed
+    tc_commit(&bars->mma_done);
+    mbar_drain(&bars->mma_done, 0);
+}
+
+// ---------------------------------------------------------------- units of two M-tiles
+
+// A unit of two M-tiles of one expert shares each B (weight) stage between two MMAs into two
+// accumulators: a stage holds A0 | A1 | B (64 KB, STAGES2 of them in the same ring memory), a
+// third fewer bytes per MMA flop than one M-tile per stage, so the same shared memory covers 1.5x
+// the MMA time. Both TMEM accumulators belong to the unit's job (columns 0..255: the first M-tile,
+// 256..511: the second), so the epilogue of a job is not overlapped with the next job's MMAs.
+constexpr int STAGES2 = 3;
+constexpr int STAGE_BYTES2 = 2 * A_BYTES + B_BYTES;
+static_assert(STAGES2 * STAGE_BYTES2 <= STAGES * STAGE_BYTES, "the two-tile ring fits the ring memory");
+static_assert(STAGES2 <= STAGES, "stage barriers");
+
+template <class LoadB>
+__device__ __forceinline__ void run_producer2(const Smem& sm, const Sched& sc, const CUtensorMap* map_a,
+                                              const int64_t* offsets, int E, int64_t R, int T, int NT, int KB,
+                                              int* status, LoadB load_b) {
+    Barriers* bars = sm.bars;
+    int stage = 0;
+    uint32_t phase = 0;
+    uint32_t pending = 0, pend_par = 0;
+    const uint64_t pol_a = make_policy<kHintA>(), pol_b = make_policy<kHintB>();
+    bool ok = true;
+    for (int u = sc.t0; ok && u < T; u += sc.tstep) {
+        int e, ntiles;
+        int64_t row0, row_end;
+        unit2_rows(sm.tile_start, offsets, E, R, u, e, row0, row_end, ntiles);
+        const uint32_t bytes = (uint32_t)(ntiles * A_BYTES + B_BYTES);
+        for (int nt = sc.n0; ok && nt < NT; nt += sc.nstep) {
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait(&bars->empty[stage], phase ^ 1, bars, status)) { ok = false; break; }
+                mbar_expect_tx(&bars->full[stage], bytes);
+                uint8_t* sa = sm.ring + stage * STAGE_BYTES2;
+                tma_load_2d_hint(sa, map_a, kb * BK, (int)row0, &bars->full[stage], pol_a);
+                if (ntiles == 2) tma_load_2d_hint(sa + A_BYTES, map_a, kb * BK, (int)(row0 + BM), &bars->full[stage], pol_a);
+                load_b(sa + 2 * A_BYTES, e, nt, kb, &bars->full[stage], pol_b);
+                pending |= 1u << stage;
+                pend_par = (pend_par & ~(1u << stage)) | (phase << stage);
+                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+            }
+        }
+    }
+    for (int s2 = 0; s2 < STAGES2; ++s2)
+        if (pending & (1u << s2)) mbar_drain(&bars->full[s2], (pend_par >> s2) & 1u);
+}
+
+// One thread of warp 1. The unit's accumulators are handed over through tfull[0] / tempty[0].
+__device__ __forceinline__ void run_mma2(const Smem& sm, const Sched& sc, uint32_t tmem, const int64_t* offsets,
+                                         int E, int64_t R, int T, int NT, int KB, int* status) {
+    Barriers* bars = sm.bars;
+    int stage = 0;
+    uint32_t phase = 0;
+    int job = 0;
+    bool ok = true;
+    for (int u = sc.t0; ok && u < T; u += sc.tstep) {
+        int e, ntiles;
+        int64_t row0, row_end;
+        unit2_rows(sm.tile_start, offsets, E, R, u, e, row0, row_end, ntiles);
+        for (int nt = sc.n0; ok && nt < NT; nt += sc.nstep, ++job) {
+            if (!mbar_wait(&bars->tempty[0], (uint32_t)(job & 1) ^ 1, bars, status)) { ok = false; break; }
+            tc_fence_after();
+            for (int kb = 0; kb < KB; ++kb) {
+                if (!mbar_wait(&bars->full[stage], phase, bars, status)) { ok = false; break; }
+                tc_fence_after();
+                const uint32_t sa = smem_addr(sm.ring + stage * STAGE_BYTES2);
+                const uint64_t a0 = smem_desc(sa), a1 = smem_desc(sa + A_BYTES), b = smem_desc(sa + 2 * A_BYTES);
+#pragma unroll
+                for (int kk = 0; kk < BK / UK; ++kk) {
+                    const uint32_t accum = (kb > 0 || kk > 0) ? 1u : 0u;
+                    tc_mma(tmem, a0 + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), accum);
+                    if (ntiles == 2) tc_mma(tmem + (uint32_t)BN, a1 + (uint64_t)(kk * 2), b + (uint64_t)(kk * 2), accum);
+                }
+                tc_commit(&bars->empty[stage]);
+                if (++stage == STAGES2) { stage = 0; phase ^= 1; }
+            }
+            if (ok) tc_commit(&bars->tfull[0]);
+        }
+    }
     tc_commit(&bars->mma_done);
     mbar_drain(&bars->mma_done, 0);
 }

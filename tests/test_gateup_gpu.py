@@ -80,6 +80,10 @@ CASES = {
     "real_widths": ([200, 0, 317, 128, 90, 250, 33, 400, 1, 255, 256, 129], 3072, 3584),
     # H / 128 N-tiles shared by min(8, H / 128) CTAs: 10 over 8 (uneven)
     "uneven_split": ([300, 77], 1280, 128),
+    # >= 512 rows per expert on average: work units of two M-tiles sharing each weight stage,
+    # with odd tile counts (9 and 5: a last unit of one tile), an empty expert and partial tiles
+    "two_tile_units": ([1100, 600, 0, 900], 256, 128),
+    "two_tile_units_real_widths": ([700, 1300], 3072, 3584),
 }
 
 
@@ -187,3 +191,34 @@ def test_gateup_single_row(sg):
     x, out = run(sg, h, w, off)
     x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h), bits_of(w).reshape(w.shape), off.numpy())
     check("gateup single row", bits_of(x), bits_of(out), x_exact, xb_ref, mag)
+
+
+@pytest.mark.slow
+def test_gateup_large_experts_full_size_sampled(sg):
+    """32 experts x 8192 rows (H = 3072, D = 3584): the two-M-tile form at full size, sampled rows
+    of the first, a middle and the last expert plus their tile and unit boundaries."""
+    E, per, H, D = 32, 8192, 3072, 3584
+    counts = [per] * E
+    gen = torch.Generator(device=DEV).manual_seed(7)
+    R = E * per
+    h = torch.empty(R, D, dtype=torch.bfloat16, device=DEV)
+    for a in range(0, R, 32768):
+        h[a:a + 32768] = torch.randn(min(32768, R - a), D, generator=gen, device=DEV).to(torch.bfloat16)
+    w = torch.empty(E, 2 * H, D, dtype=torch.bfloat16, device=DEV)
+    for e in range(E):
+        w[e] = (torch.randn(2 * H, D, generator=gen, device=DEV) * (3.0 / D ** 0.5)).to(torch.bfloat16)
+    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=DEV)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    x, out = sg.situ_glu_fwd_gateup(h, w, off, status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(13)
+    for e in (0, 17, 31):
+        local = np.unique(np.concatenate([rng.integers(0, per, 48), [0, 127, 128, 255, 256, 383, per - 1]]))
+        rows = torch.from_numpy(e * per + local).to(DEV)
+        x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h.index_select(0, rows)), bits_of(w[e]).reshape(1, 2 * H, D),
+                                                    np.array([0, len(local)], dtype=np.int64))
+        check(f"gateup 32x8192 expert {e}", bits_of(x.index_select(0, rows)), bits_of(out.index_select(0, rows)),
+              x_exact, xb_ref, mag)
+    del h, w, x, out
+    torch.cuda.empty_cache()
