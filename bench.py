@@ -376,6 +376,11 @@ def run_native(args):
     fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
     dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak)
     gateup = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak)
+    # the same kernels on few large experts (32 x 8192 rows: the tensor-bound regime)
+    dgrad_large = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak,
+                                                        rows=1 << 18, experts=32)
+    gateup_large = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak,
+                                                           rows=1 << 18, experts=32)
     adam = None if args.no_adam else time_adam(sg, dev, 3, n=args.adam_params)
 
     traffic = None
@@ -432,6 +437,8 @@ def run_native(args):
         "fp8_saved_x": fp8,
         "dgrad_fused": dgrad,
         "gateup_fused": gateup,
+        "dgrad_fused_large_experts": dgrad_large,
+        "gateup_fused_large_experts": gateup_large,
         "adam_stream": adam,
     }
     print(json.dumps(line), flush=True)
