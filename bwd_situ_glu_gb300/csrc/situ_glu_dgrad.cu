@@ -84,7 +84,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     const Sched sc = make_sched(csplit);
     uint32_t tmem;
-    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem);
+    const int T = pipeline_setup(sm, offsets, E, R, NUM_EPI_THREADS, &tmem);
     const int* tile_start = sm.tile_start;
     cluster_sync();                          // every CTA's barriers are initialised before any remote use
 

@@ -69,7 +69,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const Sched sc = make_sched(csplit);
     uint32_t tmem;
-    const int T = pipeline_setup(sm, offsets, E, NUM_EPI_THREADS, &tmem, UNIT);
+    const int T = pipeline_setup(sm, offsets, E, R, NUM_EPI_THREADS, &tmem, UNIT);
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer: B = W_gate,e and W_up,e rows nt·128 ..

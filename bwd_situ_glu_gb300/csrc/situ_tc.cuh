@@ -326,6 +326,16 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* b, uint32_t parity, 
 // Named barrier over the epilogue warps only (id 1; id 0 is __syncthreads).
 __device__ __forceinline__ void epi_barrier(int nthreads) { asm volatile("bar.sync 1, %0;" ::"r"(nthreads) : "memory"); }
 
+// Expert e's rows as [begin, end) clamped into [0, R] (end >= begin): malformed offsets can
+// neither index outside the row range nor inflate the number of tiles beyond R/BM + E.
+__device__ __forceinline__ void expert_range(const int64_t* off, int e, int64_t R, int64_t& begin, int64_t& end) {
+    int64_t a = off[e], b = off[e + 1];
+    a = a < 0 ? 0 : (a > R ? R : a);
+    b = b < a ? a : (b > R ? R : b);
+    begin = a;
+    end = b;
+}
+
 // M-tile t -> (expert, first row, end row of the expert).
 __device__ __forceinline__ void tile_rows(const int* tile_start, const int64_t* off, int E, int64_t R, int t,
                                           int& e, int64_t& row0, int64_t& row_end) {
@@ -335,8 +345,9 @@ __device__ __forceinline__ void tile_rows(const int* tile_start, const int64_t* 
         if (tile_start[mid] <= t) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    row0 = off[e] + (int64_t)(t - tile_start[e]) * BM;
-    row_end = off[e + 1] < R ? off[e + 1] : R;     // clamped: malformed offsets never index past R
+    int64_t begin;
+    expert_range(off, e, R, begin, row_end);
+    row0 = begin + (int64_t)(t - tile_start[e]) * BM;
 }
 
 // ---------------------------------------------------------------- work assignment
@@ -368,8 +379,9 @@ __device__ __forceinline__ void unit2_rows(const int* unit_start, const int64_t*
         if (unit_start[mid] <= u) lo = mid; else hi = mid - 1;
     }
     e = lo;
-    row0 = off[e] + (int64_t)(u - unit_start[e]) * 2 * BM;
-    row_end = off[e + 1] < R ? off[e + 1] : R;
+    int64_t begin;
+    expert_range(off, e, R, begin, row_end);
+    row0 = begin + (int64_t)(u - unit_start[e]) * 2 * BM;
     ntiles = row_end - row0 > BM ? 2 : 1;
 }
 
@@ -379,15 +391,16 @@ __device__ __forceinline__ void unit2_rows(const int* unit_start, const int64_t*
 // copy: counts in parallel, then one warp scans them, each lane a contiguous segment, shuffles
 // across lanes), barrier init, TMEM allocation by warp 1. Returns the number of units; *tmem
 // receives the TMEM base address.
-__device__ __forceinline__ int pipeline_setup(const Smem& sm, const int64_t* offsets, int E, int num_epi_threads,
-                                              uint32_t* tmem, int unit_tiles = 1) {
+__device__ __forceinline__ int pipeline_setup(const Smem& sm, const int64_t* offsets, int E, int64_t R,
+                                              int num_epi_threads, uint32_t* tmem, int unit_tiles = 1) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     Barriers* bars = sm.bars;
     int* tile_start = sm.tile_start;             // per expert: its first work unit
     const int64_t unit_rows = (int64_t)unit_tiles * BM;
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
-        const int64_t n = offsets[e + 1] - offsets[e];
-        tile_start[e + 1] = n > 0 ? (int)((n + unit_rows - 1) / unit_rows) : 0;
+        int64_t begin, end;
+        expert_range(offsets, e, R, begin, end);
+        tile_start[e + 1] = (int)((end - begin + unit_rows - 1) / unit_rows);
     }
     if (threadIdx.x == 0) {
         tile_start[0] = 0;

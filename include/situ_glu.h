@@ -175,7 +175,9 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
  *              expert e holds W_down,e[:, j]), so g[r,j] = Σ_d dy[r,d]·w_down_t[e,j,d]
  *   expert_offsets device, int64 [E+1]: rows of expert e are expert_offsets[e] ..
  *              expert_offsets[e+1]-1 (non-decreasing, from 0 to R; rows grouped by expert).
- *              Malformed offsets give undefined results but no access outside the buffers.
+ *              Malformed offsets (negative, decreasing, beyond R) are clamped into [0, R]: the
+ *              results of the rows they cover are undefined, but nothing is accessed outside the
+ *              buffers and the work stays bounded (at most ceil(R/128) + E row tiles).
  *   p, dx, dp  as for situ_glu_bwd_router
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.

@@ -177,3 +177,36 @@ def test_dgrad_rejects_too_many_experts(sg):
     offs[-1] = 2
     with pytest.raises(sg.SituGluError):
         sg.situ_glu_bwd_router_dgrad(x.to(DEV), dy.to(DEV), big, offs, p.to(DEV))
+
+
+def test_malformed_offsets_stay_in_bounds_and_bounded(sg):
+    """Offsets that are negative, decreasing, far beyond R or overlapping: results are undefined,
+    but both fused GEMMs return promptly with status 0 and write nothing outside their outputs
+    (guard bands of NaN bits around dx, x and out stay intact)."""
+    import time
+    R, H, D, E = 200, 256, 64, 5
+    gen = torch.Generator().manual_seed(30)
+    off = torch.tensor([0, -5, 1 << 40, 100, 50, R], dtype=torch.int64, device=DEV)
+    x = (torch.randn(R, 2 * H, generator=gen) * 3).to(torch.bfloat16).to(DEV)
+    dy = torch.randn(R, D, generator=gen).to(torch.bfloat16).to(DEV)
+    wt = (torch.randn(E, H, D, generator=gen) * 0.1).to(torch.bfloat16).to(DEV)
+    wgu = (torch.randn(E, 2 * H, D, generator=gen) * 0.1).to(torch.bfloat16).to(DEV)
+    p = torch.rand(R, generator=gen).to(DEV)
+    guard = 4096                                     # elements of NaN bits before and after each output
+    def padded(n):
+        buf = torch.full((n + 2 * guard,), -1, dtype=torch.int16, device=DEV)   # 0xFFFF: a NaN
+        return buf, buf[guard:guard + n].view(torch.bfloat16)
+    dxb, dx = padded(R * 2 * H)
+    xb_, xo = padded(R * 2 * H)
+    ob, oo = padded(R * H)
+    dp = torch.empty(R, dtype=torch.float32, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    t0 = time.time()
+    sg.situ_glu_bwd_router_dgrad(x, dy, wt, off, p, dx.view(R, 2 * H), dp, status=st)
+    h = dy                                           # [R, D] as the gate/up input
+    sg.situ_glu_fwd_gateup(h, wgu, off, xo.view(R, 2 * H), oo.view(R, H), status=st)
+    torch.cuda.synchronize()
+    assert time.time() - t0 < 30.0
+    assert int(st.item()) == 0
+    for buf, n in ((dxb, R * 2 * H), (xb_, R * 2 * H), (ob, R * H)):
+        assert bool((buf[:guard] == -1).all()) and bool((buf[guard + n:] == -1).all())
