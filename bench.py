@@ -218,8 +218,15 @@ def cpu_baseline(get_rows, R, target_s):
     n = max(n, 16)
     x, g, p = get_rows(n)
     rate, dt = oracle_rows_per_s(x, g, p)
+    # and on one core, over a sample sized to ~target_s / 4
+    n1 = int(min(n, max(16, rate / cores * target_s / 4)))
+    n1 -= n1 % 16
+    n1 = max(n1, 16)
+    rate1, dt1 = oracle_rows_per_s(x[:n1], g[:n1], p[:n1], nthreads=1)
     return {"value": rate, "unit": "rows/s", "cores": cores, "kind": "oracle",
-            "sample": f"first {n} of {R} rows (fwd then bwd+router grad, fp64, {cores} threads), {dt:.1f} s"}
+            "sample": f"first {n} of {R} rows (fwd then bwd+router grad, fp64, {cores} threads), {dt:.1f} s",
+            "single_core": {"value": rate1, "unit": "rows/s", "cores": 1,
+                            "sample": f"first {n1} rows on one thread, {dt1:.1f} s"}}
 
 
 # ---------------------------------------------------------------- reference arm
