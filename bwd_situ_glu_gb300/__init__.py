@@ -119,6 +119,8 @@ def load():
     lib.situ_glu_bwd_router_fp8.restype = cint
     lib.situ_glu_bwd_router_dgrad.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp]
     lib.situ_glu_bwd_router_dgrad.restype = cint
+    lib.situ_glu_bwd_router_dgrad_wd.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, vp, i64, i64, i64, f32, f32, vp]
+    lib.situ_glu_bwd_router_dgrad_wd.restype = cint
     lib.situ_glu_fwd_gateup.argtypes = [vp, vp, vp, i64, vp, vp, vp, i64, i64, i64, f32, f32, vp]
     lib.situ_glu_fwd_gateup.restype = cint
     lib.situ_glu_selftest_wait_timeout.argtypes = [vp, vp, vp]
@@ -362,6 +364,39 @@ def situ_glu_bwd_router_dgrad(x, dy, w_down_t, expert_offsets, p, dx=None, dp=No
     return dx, dp
 
 
+def situ_glu_bwd_router_dgrad_wd(x, dy, w_down, expert_offsets, p, dx=None, dp=None, status=None,
+                                 beta: float = 4.0, lbeta: float = 25.0, stream=None):
+    """As situ_glu_bwd_router_dgrad, with the experts' W_down in the nn.Linear layout [E, D, H]."""
+    import torch
+    if x.dim() != 2 or x.shape[1] % 2 != 0:
+        raise ValueError("x must be [R, 2H]")
+    R, H = x.shape[0], x.shape[1] // 2
+    if w_down.dim() != 3:
+        raise ValueError("w_down must be [E, D, H]")
+    E, D = w_down.shape[0], w_down.shape[1]
+    _need(x, torch.bfloat16, (R, 2 * H), "x")
+    _need(dy, torch.bfloat16, (R, D), "dy")
+    _need(w_down, torch.bfloat16, (E, D, H), "w_down")
+    _need(expert_offsets, torch.int64, (E + 1,), "expert_offsets")
+    _need(p, torch.float32, (R,), "p")
+    if dx is None:
+        dx = torch.empty((R, 2 * H), dtype=torch.bfloat16, device=x.device)
+    if dp is None:
+        dp = torch.empty((R,), dtype=torch.float32, device=x.device)
+    _need(dx, torch.bfloat16, (R, 2 * H), "dx")
+    _need(dp, torch.float32, (R,), "dp")
+    sptr = 0
+    if status is not None:
+        _need(status, torch.int32, (1,), "status")
+        sptr = status.data_ptr()
+    with torch.cuda.device(x.device):
+        _check(load().situ_glu_bwd_router_dgrad_wd(x.data_ptr(), dy.data_ptr(), w_down.data_ptr(),
+                                                   expert_offsets.data_ptr(), E, p.data_ptr(), dx.data_ptr(),
+                                                   dp.data_ptr(), sptr, R, H, D, beta, lbeta,
+                                                   _stream_handle(stream, x.device)))
+    return dx, dp
+
+
 def situ_glu_fwd_gateup(h, w_gate_up, expert_offsets, x=None, out=None, status=None, beta: float = 4.0,
                         lbeta: float = 25.0, stream=None):
     """(x bf16 [R,2H], out bf16 [R,H]) from the dispatched inputs h [R,D] and the experts' stacked
@@ -464,7 +499,7 @@ __all__ = [
     "build", "load", "version", "status_string", "SituGluError",
     "situ_glu_fwd", "situ_glu_bwd_router", "situ_glu_fwd_ptr", "situ_glu_bwd_router_ptr",
     "situ_glu_fwd_save_fp8", "situ_glu_bwd_router_fp8", "FP8_BLOCK", "fp8_scale_blocks",
-    "situ_glu_bwd_router_dgrad", "situ_glu_fwd_gateup",
+    "situ_glu_bwd_router_dgrad", "situ_glu_bwd_router_dgrad_wd", "situ_glu_fwd_gateup",
     "situ_and_mul", "selftest_wait_timeout", "AdamParams", "adam_params", "situ_adam_update_host", "situ_adam_stream_step", "adam_staging_bytes",
     "LIB_PATH", "INCLUDE",
 ]

@@ -59,7 +59,10 @@ static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
 
 // ---------------------------------------------------------------- the kernel
 
-template <bool BETA4>
+// W_MN: the weights arrive as W_down,e [D, H] (the nn.Linear layout: N-major for this GEMM),
+// loaded as four 64-column boxes per stage and read by the MMA with B transposed; otherwise as
+// (W_down,e)ᵀ [H, D] (K-major), one 256-row box per stage.
+template <bool BETA4, bool W_MN>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     dgrad_bwd_kernel(const __grid_constant__ CUtensorMap map_dy, const __grid_constant__ CUtensorMap map_w,
                      const uint16_t* __restrict__ x, const int64_t* __restrict__ offsets, const float* __restrict__ p,
@@ -93,12 +96,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0)
             run_producer(sm, sc, &map_dy, offsets, E, R, T, NT, KB, status,
                          [&](uint8_t* sb, int e, int nt, int kb, uint64_t* bar, uint64_t pol) {
-                             tma_load_2d_hint(sb, &map_w, kb * BK, (int)((int64_t)e * H + (int64_t)nt * BN), bar,
-                                              pol);
+                             if constexpr (W_MN) {
+                                 // rows e·D + kb·64 .. of W_down,e, columns nt·256 + 64j ..
+                                 const int r = (int)((int64_t)e * (KB * BK) + (int64_t)kb * BK);
+#pragma unroll
+                                 for (int j = 0; j < BN / 64; ++j)
+                                     tma_load_2d_hint(sb + j * BMN_BOX_BYTES, &map_w, nt * BN + 64 * j, r, bar, pol);
+                             } else {
+                                 tma_load_2d_hint(sb, &map_w, kb * BK, (int)((int64_t)e * H + (int64_t)nt * BN),
+                                                  bar, pol);
+                             }
                          });
     } else if (warp == 1) {
         // ------------------------------------------------ MMA issuer
-        if (lane == 0) run_mma(sm, sc, tmem, T, NT, KB, status);
+        if (lane == 0) run_mma<W_MN>(sm, sc, tmem, T, NT, KB, status);
     } else {
         // ------------------------------------------------ epilogue (warps 2 .. 2 + 4·EPW − 1)
         // A warp may read only the TMEM lanes of quadrant warp % 4; the EPW warps of a quadrant take
@@ -213,21 +224,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 }  // namespace
 
-extern "C" {
+namespace {
 
-int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_t, const int64_t* expert_offsets,
-                              int64_t E, const float* p, void* dx, float* dp, int* status, int64_t R, int64_t H,
-                              int64_t D, float beta, float lbeta, cudaStream_t stream) {
+// Both entry points: w is (W_down,e)ᵀ [E, H, D] (w_mn false) or W_down,e [E, D, H] (w_mn true).
+int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const int64_t* expert_offsets, int64_t E,
+                 const float* p, void* dx, float* dp, int* status, int64_t R, int64_t H, int64_t D, float beta,
+                 float lbeta, cudaStream_t stream) {
     int st = check_shape(R, H, beta, lbeta);
     if (st != SITU_GLU_OK) return st;
     if (D <= 0 || D % BK != 0 || H % BN != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
-    if (R > INT32_MAX || E * H > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
+    if (R > INT32_MAX || E * H > INT32_MAX || E * D > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
     if (R == 0) return SITU_GLU_OK;
-    if (!x || !dy || !w_down_t || !expert_offsets || !p || !dx || !dp) return SITU_GLU_INVALID_ARG;
-    if (!aligned(x, 32) || !aligned(dy, 16) || !aligned(w_down_t, 16) || !aligned(dx, 32) ||
+    if (!x || !dy || !w || !expert_offsets || !p || !dx || !dp) return SITU_GLU_INVALID_ARG;
+    if (!aligned(x, 32) || !aligned(dy, 16) || !aligned(w, 16) || !aligned(dx, 32) ||
         !aligned(expert_offsets, 8) || !aligned(p, 4) || !aligned(dp, 4) || (status && !aligned(status, 4)))
         return SITU_GLU_INVALID_ARG;
-    const Range rx = range_of(x, R * 2 * H * 2), ry = range_of(dy, R * D * 2), rw = range_of(w_down_t, E * H * D * 2);
+    const Range rx = range_of(x, R * 2 * H * 2), ry = range_of(dy, R * D * 2), rw = range_of(w, E * H * D * 2);
     const Range ro = range_of(expert_offsets, (E + 1) * 8), rp = range_of(p, R * 4);
     const Range rdx = range_of(dx, R * 2 * H * 2), rdp = range_of(dp, R * 4);
     for (Range in : {rx, ry, rw, ro, rp}) {
@@ -239,11 +251,14 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
 
     CUtensorMap map_dy, map_w;
     if (!make_map(&map_dy, dy, (uint64_t)R, (uint64_t)D, BM)) return cuda_fail(cudaErrorInvalidValue);
-    if (!make_map(&map_w, w_down_t, (uint64_t)(E * H), (uint64_t)D, BN)) return cuda_fail(cudaErrorInvalidValue);
+    const bool mw = w_mn ? make_map(&map_w, w, (uint64_t)(E * D), (uint64_t)H, BK, 64)    // 64 K rows x 64 N
+                         : make_map(&map_w, w, (uint64_t)(E * H), (uint64_t)D, BN);       // 256 N rows x 64 K
+    if (!mw) return cuda_fail(cudaErrorInvalidValue);
 
     const Coef c = make_coef(beta, lbeta);
     const bool b4 = fast_path(beta, lbeta);
-    auto kernel = b4 ? dgrad_bwd_kernel<true> : dgrad_bwd_kernel<false>;
+    auto kernel = b4 ? (w_mn ? dgrad_bwd_kernel<true, true> : dgrad_bwd_kernel<true, false>)
+                     : (w_mn ? dgrad_bwd_kernel<false, true> : dgrad_bwd_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e);
     const int NT = (int)(H / BN);
@@ -254,6 +269,22 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return SITU_GLU_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_t, const int64_t* expert_offsets,
+                              int64_t E, const float* p, void* dx, float* dp, int* status, int64_t R, int64_t H,
+                              int64_t D, float beta, float lbeta, cudaStream_t stream) {
+    return dgrad_launch(x, dy, w_down_t, false, expert_offsets, E, p, dx, dp, status, R, H, D, beta, lbeta, stream);
+}
+
+int situ_glu_bwd_router_dgrad_wd(const void* x, const void* dy, const void* w_down, const int64_t* expert_offsets,
+                                 int64_t E, const float* p, void* dx, float* dp, int* status, int64_t R, int64_t H,
+                                 int64_t D, float beta, float lbeta, cudaStream_t stream) {
+    return dgrad_launch(x, dy, w_down, true, expert_offsets, E, p, dx, dp, status, R, H, D, beta, lbeta, stream);
 }
 
 }  // extern "C"

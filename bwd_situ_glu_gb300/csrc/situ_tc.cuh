@@ -210,11 +210,30 @@ constexpr uint32_t IDESC = (1u << 4)           // D format fp32
                          | ((uint32_t)(BN >> 3) << 17)
                          | ((uint32_t)(BM >> 4) << 24);
 
+// The same with B stored N-major ("MN-major": bit 16, transpose B).
+constexpr uint32_t IDESC_BMN = IDESC | (1u << 16);
+
+// Shared-memory descriptor of an N-major bf16 B tile with 128-byte swizzle, as written by TMA
+// boxes of 64 N-elements x 64 K-rows: each K row of a box is 128 bytes (64 consecutive N), 8 K
+// rows form a 1024-byte swizzle atom (stride byte offset), and the next 64 N-elements start one
+// box (8 KB) further on (leading byte offset).
+constexpr uint32_t BMN_BOX_BYTES = 64 * BK * 2;
+__device__ __forceinline__ uint64_t smem_desc_mn(uint32_t saddr) {
+    uint64_t d = 0;
+    d |= (uint64_t)((saddr >> 4) & 0x3FFFu);
+    d |= (uint64_t)((BMN_BOX_BYTES >> 4) & 0x3FFFu) << 16;   // leading byte offset: next 64 N
+    d |= (uint64_t)(1024 >> 4) << 32;                         // stride byte offset: next 8 K rows
+    d |= (uint64_t)1 << 46;
+    d |= (uint64_t)2 << 61;
+    return d;
+}
+
+template <bool B_MN = false>
 __device__ __forceinline__ void tc_mma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t accumulate) {
     asm volatile(
         "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}" ::"r"(
             d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(IDESC), "r"(accumulate)
+        "l"(adesc), "l"(bdesc), "r"(B_MN ? IDESC_BMN : IDESC), "r"(accumulate)
         : "memory");
 }
 
@@ -484,7 +503,8 @@ __device__ __forceinline__ void run_producer(const Smem& sm, const Sched& sc, co
     }
 }
 
-// One thread of warp 1: the MMA issuer.
+// One thread of warp 1: the MMA issuer. B_MN: the B tile is N-major (four 64-column TMA boxes).
+template <bool B_MN = false>
 __device__ __forceinline__ void run_mma(const Smem& sm, const Sched& sc, uint32_t tmem, int T, int NT, int KB,
                                         int* status) {
     Barriers* bars = sm.bars;
@@ -503,11 +523,14 @@ __device__ __forceinline__ void run_mma(const Smem& sm, const Sched& sc, uint32_
                 if (!mbar_wait(&bars->full[stage], phase, bars, status)) { ok = false; break; }
                 tc_fence_after();
                 const uint32_t sa = smem_addr(sm.ring + stage * STAGE_BYTES);
-                const uint64_t adesc = smem_desc(sa), bdesc = smem_desc(sa + A_BYTES);
+                const uint64_t adesc = smem_desc(sa);
+                const uint64_t bdesc = B_MN ? smem_desc_mn(sa + A_BYTES) : smem_desc(sa + A_BYTES);
 #pragma unroll
                 for (int kk = 0; kk < BK / UK; ++kk) {
-                    // advance 16 bf16 (32 bytes = 2 descriptor units) along K inside the swizzled rows
-                    tc_mma(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + (uint64_t)(kk * 2), (kb > 0 || kk > 0) ? 1u : 0u);
+                    // A (K-major): advance 16 bf16 = 32 bytes (2 descriptor units) inside the swizzled
+                    // rows; B N-major: advance 16 K rows = 2048 bytes (128 units) to the next two atoms
+                    const uint64_t bk = B_MN ? (uint64_t)(kk * 128) : (uint64_t)(kk * 2);
+                    tc_mma<B_MN>(d_tmem, adesc + (uint64_t)(kk * 2), bdesc + bk, (kb > 0 || kk > 0) ? 1u : 0u);
                 }
                 tc_commit(&bars->empty[stage]);          // ring stage free once these MMAs finish
                 if (++stage == STAGES) { stage = 0; phase ^= 1; }

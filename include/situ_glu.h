@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 4
+#define SITU_GLU_VERSION_MINOR 5
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -191,6 +191,15 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
                               const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
                               float* dp, int* status, int64_t R, int64_t H, int64_t D, float beta,
                               float lbeta, cudaStream_t stream);
+
+/* The same with the weights in their nn.Linear layout: w_down device, bf16 [E,D,H], row d of
+ * expert e holding W_down,e[d, :], so g[r,j] = Σ_d dy[r,d]·w_down[e,d,j] (read N-major by the
+ * tensor cores; no transposed copy needed). E*D < 2^31; everything else as above; results are
+ * bit-identical to situ_glu_bwd_router_dgrad on the transposed weights. */
+int situ_glu_bwd_router_dgrad_wd(const void* x, const void* dy, const void* w_down,
+                                 const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
+                                 float* dp, int* status, int64_t R, int64_t H, int64_t D,
+                                 float beta, float lbeta, cudaStream_t stream);
 
 /* ---------------------------------------------------------------------------------------
  * Gate/up projection fused with the forward (tensor cores).

@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10400
+    assert sg.version() == 10500
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
@@ -238,3 +238,15 @@ def test_selftest_validates(lib):
     assert lib.situ_glu_selftest_wait_timeout(None, None, None) == INVALID
     assert lib.situ_glu_selftest_wait_timeout(A + 2, None, None) == INVALID        # status needs 4 bytes
     assert lib.situ_glu_selftest_wait_timeout(A, A + 4, None) == INVALID           # elapsed needs 8 bytes
+
+
+def test_dgrad_wd_validates_before_any_launch(lib):
+    R, H, D, E = 4, 256, 64, 2
+    x, dy, w, off, p = A, A + (1 << 20), A + (2 << 20), A + (3 << 20), A + (4 << 20)
+    dx, dp, st = B, B + (1 << 20), B + (2 << 20)
+    f = lambda *a: lib.situ_glu_bwd_router_dgrad_wd(*a, None)
+    assert f(None, None, None, None, E, None, None, None, None, 0, H, D, 4.0, 25.0) == OK
+    assert f(x, dy, w, off, E, p, dx, dp, st, R, 128, D, 4.0, 25.0) == INVALID          # H % 256
+    assert f(x, dy, w, off, E, p, dx, dp, st, R, H, 96, 4.0, 25.0) == INVALID           # D % 64
+    assert f(x, dy, w + 8, off, E, p, dx, dp, st, R, H, D, 4.0, 25.0) == INVALID        # w 16-byte aligned
+    assert f(x, dy, w, off, E, p, w + 64, dp, st, R, H, D, 4.0, 25.0) == OVERLAP        # dx over w

@@ -210,3 +210,26 @@ def test_malformed_offsets_stay_in_bounds_and_bounded(sg):
     assert int(st.item()) == 0
     for buf, n in ((dxb, R * 2 * H), (xb_, R * 2 * H), (ob, R * H)):
         assert bool((buf[:guard] == -1).all()) and bool((buf[guard + n:] == -1).all())
+
+
+@pytest.mark.parametrize("name", ["partial_tiles", "empty_experts", "uneven_split", "real_widths"])
+def test_dgrad_nn_linear_weight_layout(sg, name):
+    """W_down in its nn.Linear layout [E, D, H] (read N-major by the tensor cores) gives exactly
+    the results of the transposed weights [E, H, D]; and both match the oracle."""
+    counts, H, D = CASES[name]
+    x, dy, wt, off, p = make(counts, H, D, seed=len(name) + 50)
+    wd = wt.transpose(1, 2).contiguous()                      # [E, D, H]
+    dx1, dp1 = run(sg, x, dy, wt, off, p)
+    status = torch.zeros(1, dtype=torch.int32, device=DEV)
+    dx2, dp2 = sg.situ_glu_bwd_router_dgrad_wd(x.to(DEV), dy.to(DEV), wd.to(DEV), off.to(DEV), p.to(DEV),
+                                               status=status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(dx1.view(torch.int16), dx2.view(torch.int16))
+    assert torch.equal(dp1.view(torch.int32), dp2.view(torch.int32))
+    dx_ref, dp_ref, dpa = oracle.dgrad_bwd_router(bits_of(x), bits_of(dy), bits_of(wt).reshape(wt.shape),
+                                                 off.numpy(), p.numpy())
+    par = Parity("dgrad nn.Linear layout " + name)
+    par.bf16("dx", bits_of(dx2), dx_ref)
+    par.dp(dp2.cpu().numpy(), dp_ref, dpa)
+    par.assert_ok()
