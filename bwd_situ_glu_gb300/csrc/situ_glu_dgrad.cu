@@ -49,8 +49,16 @@ constexpr bool buffers_ok() {                // a slot's last chunk of a job nev
     return true;
 }
 static_assert(buffers_ok(), "x buffer rotation across job boundaries");
-constexpr int DGRAD_SPLIT = 4;               // CTAs per cluster sharing an M-tile (each every 4th N-tile)
-constexpr int MAX_SPLIT = DGRAD_SPLIT;
+constexpr int DGRAD_SPLIT = 4;               // CTAs sharing an M-tile (each every 4th N-tile)
+// The CTAs sharing an M-tile form one cluster (their dp partials meet in the leader's shared
+// memory) when the experts are large; with small experts they form two clusters of 2, which fill
+// all 152 SMs where clusters of 4 leave 8 idle (GPC packing), and the two cluster sums meet in dp.
+// Measured at R = 262144, H = 3072, D = 3584: 896 experts of ~292 rows 8.03 ms (one cluster of 4)
+// vs 7.25 ms (two of 2); 32 experts of 8192 rows 4.52 vs 4.73 ms.
+constexpr int DGRAD_CLUSTER = 2;
+constexpr int64_t CLUSTER4_MIN_ROWS = 4 * BM; // experts averaging at least this many rows: clusters of 4
+static_assert(DGRAD_SPLIT / DGRAD_CLUSTER <= 2, "at most two dp contributions per row: a + b == b + a");
+constexpr int MAX_SPLIT = DGRAD_SPLIT;       // largest cluster
 // extra shared memory: dp_part [EPW][BM] | dp_cl [2][MAX_SPLIT][BM] | dp_full[2], dp_free[2]
 constexpr int SMEM_BYTES = SMEM_FIXED_BYTES + 16 + EPW * BM * 4 + 2 * MAX_SPLIT * BM * 4 + 4 * 8;
 static_assert(SMEM_BYTES <= 232448, "shared memory per CTA");
@@ -67,7 +75,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     dgrad_bwd_kernel(const __grid_constant__ CUtensorMap map_dy, const __grid_constant__ CUtensorMap map_w,
                      const uint16_t* __restrict__ x, const int64_t* __restrict__ offsets, const float* __restrict__ p,
                      uint16_t* __restrict__ dx, float* __restrict__ dp, int* __restrict__ status, int E, int64_t R,
-                     int64_t H, int KB, int csplit, Coef c) {
+                     int64_t H, int KB, int csplit, int ncl, Coef c) {
     extern __shared__ uint8_t smem_raw[];
     const Smem sm = carve_smem(smem_raw);
     Barriers* bars = sm.bars;
@@ -81,7 +89,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (threadIdx.x == 0) {
         for (int b = 0; b < 2; ++b) {
-            mbar_init(&dp_full[b], (uint32_t)((csplit - 1) * BM));
+            mbar_init(&dp_full[b], (uint32_t)((ncl - 1) * BM));
             mbar_init(&dp_free[b], (uint32_t)BM);
         }
     }
@@ -190,16 +198,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            // combine the EPW column slices of each row, then the csplit CTAs of the cluster: every
+            // combine the EPW column slices of each row, then the ncl CTAs of the cluster: every
             // rank pushes its partial into the leader's shared memory (double-buffered by M-tile
-            // parity) and the leader adds them in rank order, so dp does not depend on timing
+            // parity) and the leader adds them in rank order. When the csplit CTAs of the M-tile form
+            // two clusters, each leader adds its cluster's sum into the zeroed dp with one
+            // red.global.add: two addends commute exactly, so dp does not depend on timing either way
             if (slot > 0) dp_part[slot * BM + lrow] = acc_dp;
             epi_barrier(NUM_EPI_THREADS);
             if (slot == 0) {
                 float s = acc_dp;
 #pragma unroll
                 for (int k = 1; k < EPW; ++k) s += dp_part[k * BM + lrow];
-                if (csplit > 1) {
+                if (ncl > 1) {
                     const int b = it & 1;
                     const uint32_t use_par = (uint32_t)((it >> 1) & 1);
                     if (crank != 0) {
@@ -208,11 +218,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         mbar_arrive_cluster(cluster_addr(&dp_full[b], 0));
                     } else {
                         mbar_wait_cluster(&dp_full[b], use_par, bars, status);
-                        for (int k = 1; k < csplit; ++k) s += dp_cl[(b * MAX_SPLIT + k) * BM + lrow];
-                        for (int k = 1; k < csplit; ++k) mbar_arrive_cluster(cluster_addr(&dp_free[b], (uint32_t)k));
+                        for (int k = 1; k < ncl; ++k) s += dp_cl[(b * MAX_SPLIT + k) * BM + lrow];
+                        for (int k = 1; k < ncl; ++k) mbar_arrive_cluster(cluster_addr(&dp_free[b], (uint32_t)k));
                     }
                 }
-                if (crank == 0 && valid) dp[row] = 16.0f * s;
+                if (crank == 0 && valid) {
+                    if (ncl < csplit) atomicAdd(&dp[row], 16.0f * s);
+                    else dp[row] = 16.0f * s;
+                }
             }
             epi_barrier(NUM_EPI_THREADS);
         }
@@ -263,8 +276,14 @@ int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const 
     if (e != cudaSuccess) return cuda_fail(e);
     const int NT = (int)(H / BN);
     const int csplit = NT < DGRAD_SPLIT ? NT : DGRAD_SPLIT;
-    e = launch_clusters(kernel, R, E, csplit, NUM_THREADS, SMEM_BYTES, stream, map_dy, map_w, (const uint16_t*)x,
-                        expert_offsets, p, (uint16_t*)dx, dp, status, (int)E, R, H, (int)(D / BK), csplit, c);
+    const int ncl = (csplit % DGRAD_CLUSTER != 0 || R / E >= CLUSTER4_MIN_ROWS) ? csplit : DGRAD_CLUSTER;
+    if (ncl < csplit) {                      // two clusters per M-tile add into dp
+        e = cudaMemsetAsync(dp, 0, (size_t)R * 4, stream);
+        if (e != cudaSuccess) return cuda_fail(e);
+    }
+    e = launch_clusters(kernel, R, E, ncl, csplit, NUM_THREADS, SMEM_BYTES, stream, map_dy, map_w,
+                        (const uint16_t*)x, expert_offsets, p, (uint16_t*)dx, dp, status, (int)E, R, H,
+                        (int)(D / BK), csplit, ncl, c);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);

@@ -670,15 +670,18 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Launch of a persistent kernel as clusters of csplit CTAs (csplit = 1: plain CTAs): as many
-// clusters as can be resident at once, never more than there are M-tiles.
+// Launch of a persistent kernel as clusters of ncl CTAs (ncl = 1: plain CTAs) in groups of csplit
+// CTAs (a multiple of ncl; the CTAs sharing an M-tile): as many whole groups as can be resident at
+// once, never more groups than there are M-tiles.
 template <class... KArgs, class... Args>
-inline cudaError_t launch_clusters(void (*kernel)(KArgs...), int64_t R, int64_t E, int csplit, int threads,
-                                   int smem, cudaStream_t stream, Args... args) {
+inline cudaError_t launch_clusters(void (*kernel)(KArgs...), int64_t R, int64_t E, int ncl, int csplit,
+                                   int threads, int smem, cudaStream_t stream, Args... args) {
+    if (ncl < 1 || csplit % ncl != 0) return cudaErrorInvalidConfiguration;
+    const int per_group = csplit / ncl;      // clusters per group
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = (unsigned)csplit;
+    attr[0].val.clusterDim.x = (unsigned)ncl;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.blockDim = dim3((unsigned)threads);
@@ -694,10 +697,11 @@ inline cudaError_t launch_clusters(void (*kernel)(KArgs...), int64_t R, int64_t 
     int clusters = 0;
     e = cudaOccupancyMaxActiveClusters(&clusters, (const void*)kernel, &cfg);
     if (e != cudaSuccess) return e;
-    if (clusters < 1) return cudaErrorInvalidConfiguration;
+    int64_t groups = clusters / per_group;
     const int64_t tiles = (R + BM - 1) / BM + E;
-    if (clusters > tiles) clusters = (int)tiles;
-    cfg.gridDim = dim3((unsigned)(clusters * csplit));
+    if (groups > tiles) groups = tiles;
+    if (groups < 1) return cudaErrorInvalidConfiguration;
+    cfg.gridDim = dim3((unsigned)(groups * csplit));
     return cudaLaunchKernelEx(&cfg, kernel, args...);
 }
 

@@ -178,7 +178,10 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
  *              Malformed offsets (negative, decreasing, beyond R) are clamped into [0, R]: the
  *              results of the rows they cover are undefined, but nothing is accessed outside the
  *              buffers and the work stays bounded (at most ceil(R/128) + E row tiles).
- *   p, dx, dp  as for situ_glu_bwd_router
+ *   p, dx, dp  as for situ_glu_bwd_router. When H >= 1024 and the experts average fewer than
+ *              512 rows, dp is zeroed on the stream first and each row's dp arrives as two
+ *              partial sums added with atomics; two addends commute exactly, so dp is still
+ *              deterministic (that add flushes a subnormal result, |dp| < 2^-126, to zero).
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.
  *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 1024, R < 2^31, E*H < 2^31

@@ -45,9 +45,12 @@ CASES = {
     "partial_tiles": ([100, 60], 256, 128),
     "empty_experts": ([0, 300, 1, 129, 0, 77, 0], 512, 256),
     "real_widths": ([200, 0, 317, 128, 90, 250, 33, 400, 1, 255, 256, 129], 3072, 3584),
-    # H / 256 N-tiles shared by a cluster of min(4, H / 256) CTAs: 3 of 3, and 5 over 4 (uneven)
+    # H / 256 N-tiles shared by min(4, H / 256) CTAs (one cluster of 3; four CTAs as two clusters
+    # of 2, or as one cluster of 4 when the experts average 512 rows or more): 3 of 3, 5 over 4
+    # (uneven), and 4 over one cluster of 4
     "three_way_split": ([129, 0, 200], 768, 64),
     "uneven_split": ([300, 77], 1280, 128),
+    "large_experts": ([600, 517, 1000], 1024, 128),
 }
 
 
@@ -212,7 +215,18 @@ def test_malformed_offsets_stay_in_bounds_and_bounded(sg):
         assert bool((buf[:guard] == -1).all()) and bool((buf[guard + n:] == -1).all())
 
 
-@pytest.mark.parametrize("name", ["partial_tiles", "empty_experts", "uneven_split", "real_widths"])
+def test_dgrad_dp_is_deterministic(sg):
+    """Four CTAs share each M-tile as two clusters of two, and the two cluster sums meet in dp
+    through atomic adds: two addends commute exactly, so repeated runs give bit-identical dp."""
+    counts, H, D = CASES["real_widths"]
+    x, dy, wt, off, p = make(counts, H, D, seed=77)
+    runs = [run(sg, x, dy, wt, off, p) for _ in range(3)]
+    for dx, dp in runs[1:]:
+        assert torch.equal(dx.view(torch.int16), runs[0][0].view(torch.int16))
+        assert torch.equal(dp.view(torch.int32), runs[0][1].view(torch.int32))
+
+
+@pytest.mark.parametrize("name", ["partial_tiles", "empty_experts", "uneven_split", "real_widths", "large_experts"])
 def test_dgrad_nn_linear_weight_layout(sg, name):
     """W_down in its nn.Linear layout [E, D, H] (read N-major by the tensor cores) gives exactly
     the results of the transposed weights [E, H, D]; and both match the oracle."""
