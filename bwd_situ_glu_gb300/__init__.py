@@ -10,6 +10,16 @@ Binding names match the C entry points:
 
 * ``situ_glu_fwd(x, out=None, beta=4.0, lbeta=25.0, stream=None) -> out``
 * ``situ_glu_bwd_router(x, g, p, dx=None, dp=None, beta=4.0, lbeta=25.0, stream=None) -> (dx, dp)``
+* ``situ_glu_fwd_save_fp8`` / ``situ_glu_bwd_router_fp8``: the same with x saved as block-wise
+  FP8 (E4M3 codes + fp32 scales of 128-element blocks)
+* ``situ_glu_bwd_router_dgrad`` / ``situ_glu_bwd_router_dgrad_wd``: g = dY·W_down,e per expert on
+  the tensor cores with the backward in the GEMM's epilogue (weights [E, H, D] or [E, D, H])
+* ``situ_glu_fwd_gateup``: x = [W_gate,e·h | W_up,e·h] per expert on the tensor cores with the
+  forward in the GEMM's epilogue
+* ``situ_adam_update_host`` / ``situ_adam_stream_step``: Adam on host-resident state, the
+  streamed form moving gradients and weights chunk by chunk
+* ``situ_and_mul(x, beta, linear_beta)``: autograd function (forward kernel; backward kernel
+  with p = 1), the pages' operator interface
 
 Shapes: ``x`` bf16 [R, 2H] (gate | linear), ``g`` bf16 [R, H], ``p`` fp32 [R];
 ``out`` bf16 [R, H], ``dx`` bf16 [R, 2H], ``dp`` fp32 [R]. All on one CUDA device.
