@@ -49,6 +49,11 @@ constexpr bool buffers_ok() {                // a slot's last chunk of a job nev
     return true;
 }
 static_assert(buffers_ok(), "x buffer rotation across job boundaries");
+// L2 sector promotion of the operand loads. The weight tiles with 128-byte promotion instead of
+// 256: 5-6 % faster at both shapes (896 experts x ~292 rows 7.22-7.27 -> 6.85-6.93 ms, 32 x 8192
+// rows 4.49-4.51 -> 4.22 ms, same call); for the dY tiles it makes no measurable difference.
+constexpr CUtensorMapL2promotion DGRAD_L2_PROMO_A = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;   // dY tiles
+constexpr CUtensorMapL2promotion DGRAD_L2_PROMO_B = CU_TENSOR_MAP_L2_PROMOTION_L2_128B;   // weight tiles
 constexpr int DGRAD_SPLIT = 4;               // CTAs sharing an M-tile (each every 4th N-tile)
 // The CTAs sharing an M-tile form one cluster (their dp partials meet in the leader's shared
 // memory) when the experts are large; with small experts they form two clusters of 2, which fill
@@ -263,9 +268,12 @@ int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const 
     if (status && (overlap(range_of(status, 4), rdx) || overlap(range_of(status, 4), rdp))) return SITU_GLU_OVERLAP;
 
     CUtensorMap map_dy, map_w;
-    if (!make_map(&map_dy, dy, (uint64_t)R, (uint64_t)D, BM)) return cuda_fail(cudaErrorInvalidValue);
-    const bool mw = w_mn ? make_map(&map_w, w, (uint64_t)(E * D), (uint64_t)H, BK, 64)    // 64 K rows x 64 N
-                         : make_map(&map_w, w, (uint64_t)(E * H), (uint64_t)D, BN);       // 256 N rows x 64 K
+    if (!make_map(&map_dy, dy, (uint64_t)R, (uint64_t)D, BM, BK, true, DGRAD_L2_PROMO_A))
+        return cuda_fail(cudaErrorInvalidValue);
+    const bool mw = w_mn ? make_map(&map_w, w, (uint64_t)(E * D), (uint64_t)H, BK, 64, true,   // 64 K rows x 64 N
+                                    DGRAD_L2_PROMO_B)
+                         : make_map(&map_w, w, (uint64_t)(E * H), (uint64_t)D, BN, BK, true,   // 256 N rows x 64 K
+                                    DGRAD_L2_PROMO_B);
     if (!mw) return cuda_fail(cudaErrorInvalidValue);
 
     const Coef c = make_coef(beta, lbeta);

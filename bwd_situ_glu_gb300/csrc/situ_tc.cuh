@@ -144,6 +144,16 @@ __device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* m
         : "memory");
 }
 
+// 3-D box load (dims innermost first) with an L2 eviction-priority policy.
+__device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                                 uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1, {%2, "
+        "%3, %4}], [%5], %6;" ::"r"(smem_addr(dst)),
+        "l"(map), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
 enum class L2Hint { normal, first, last };
 
 template <L2Hint P>
@@ -656,9 +666,11 @@ inline EncodeTiled encode_fn() {
 
 // 2-D bf16 tensor map: rows x cols (cols contiguous), box of box_rows x box_cols. Operand tiles use
 // 64 columns (128 bytes) with the 128-byte swizzle the MMA descriptors expect; epilogue output
-// tiles are unswizzled. Rows past the end read as zero and are not written.
+// tiles are unswizzled. Rows past the end read as zero and are not written. promo: the L2 sector
+// promotion of the box's reads (256 bytes unless a kernel measured better with less).
 inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
-                     uint32_t box_cols = BK, bool swizzle128 = true) {
+                     uint32_t box_cols = BK, bool swizzle128 = true,
+                     CUtensorMapL2promotion promo = CU_TENSOR_MAP_L2_PROMOTION_L2_256B) {
     EncodeTiled fn = encode_fn();
     if (!fn) return false;
     const cuuint64_t dims[2] = {cols, rows};
@@ -667,7 +679,22 @@ inline bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint64_t c
     const cuuint32_t estr[2] = {1, 1};
     return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+              promo, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D bf16 tensor map, 128-byte swizzle: d0 (contiguous) x d1 (stride1 bytes) x d2 (stride2
+// bytes), box of box0 x box1 x box2 (box0 = 64: one 128-byte swizzle row).
+inline bool make_map_3d(CUtensorMap* m, const void* base, uint64_t d0, uint64_t d1, uint64_t d2, uint64_t stride1,
+                        uint64_t stride2, uint32_t box0, uint32_t box1, uint32_t box2) {
+    EncodeTiled fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[3] = {d0, d1, d2};
+    const cuuint64_t strides[2] = {stride1, stride2};
+    const cuuint32_t box[3] = {box0, box1, box2};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // Launch of a persistent kernel as clusters of ncl CTAs (ncl = 1: plain CTAs) in groups of csplit
