@@ -425,9 +425,11 @@ def run_native(args):
                    "parallelism": f"replicas x{world} (rows shard, no collective)",
                    "l2": "inputs larger than L2 (x alone is %.2f GB vs 129 MB L2); no flush" % (4 * H * R / 1e9)},
         "passes": {
-            "fwd": {"ms": fwd_avg, "GB_s": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
+            "fwd": {"ms": fwd_avg, "ms_median": statistics.median(fwd_ms), "ms_min": min(fwd_ms),
+                    "GB_s": fwd_gbs, "frac_of_peak": fwd_gbs / peak,
                     "rows_per_s": R / (fwd_avg * 1e-3), "bytes": fwd_bytes},
-            "bwd_router": {"ms": bwd_avg, "GB_s": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
+            "bwd_router": {"ms": bwd_avg, "ms_median": statistics.median(bwd_ms), "ms_min": min(bwd_ms),
+                           "GB_s": bwd_gbs, "frac_of_peak": bwd_gbs / peak,
                            "rows_per_s": R / (bwd_avg * 1e-3), "bytes": bwd_bytes},
             "step_GB_s": step_gbs,
         },
