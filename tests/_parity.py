@@ -30,14 +30,28 @@ def bits_of(t: torch.Tensor) -> np.ndarray:
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
-    return (b.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    return np.left_shift(b, 16, dtype=np.uint32).view(np.float32).astype(np.float64)
 
 
-def ulp_bf16(ref: np.ndarray) -> np.ndarray:
+def ulp_bf16_reference(ref: np.ndarray) -> np.ndarray:
+    """2^(floor(log2|ref|) - 7), 0 for ref == 0: the definition, through frexp (slow)."""
     mag = np.abs(ref)
     _, e = np.frexp(mag)                 # mag = m·2^e, m in [0.5, 1)  ->  floor(log2 mag) = e - 1
     u = np.ldexp(1.0, (e - 8).astype(np.int32))
     return np.where(mag == 0, 0.0, u)
+
+
+def ulp_bf16(ref: np.ndarray) -> np.ndarray:
+    """The same from the float64 exponent field: for a normal double of biased exponent b,
+    floor(log2|ref|) = b - 1023, so the ulp is the double with exponent field b - 7 and a zero
+    mantissa. Doubles with b < 8 (|ref| < 2^-1016, including 0 and subnormals, all far below
+    the 1e-3 floor of the tolerance) give 0; NaN and infinity give 2^-8 as frexp's exponent 0
+    does in the definition."""
+    ref = np.ascontiguousarray(ref, dtype=np.float64)
+    b = (ref.view(np.uint64) >> np.uint64(52)) & np.uint64(0x7FF)
+    u = ((np.maximum(b, np.uint64(8)) - np.uint64(7)) << np.uint64(52)).view(np.float64)
+    u = np.where(b < 8, 0.0, u)
+    return np.where(b == 0x7FF, 2.0 ** -8, u)
 
 
 @dataclass
@@ -138,6 +152,48 @@ def compare_full(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, chunk_
         compare_rows(par, x[r0:r1], None if g is None else g[r0:r1], None if p is None else p[r0:r1],
                      None if out is None else out[r0:r1], None if dx is None else dx[r0:r1],
                      None if dp is None else dp[r0:r1], beta, lbeta, row0=r0)
+
+
+def merge(into: Parity, part: Parity):
+    """Add the tallies of `part` (a disjoint block of rows) to `into`."""
+    for k, a in into.t.items():
+        b = part.t[k]
+        a.n += b.n
+        a.bad += b.bad
+        a.worst_ratio = max(a.worst_ratio, b.worst_ratio)
+        a.worst_abs = max(a.worst_abs, b.worst_abs)
+        a.examples.extend(b.examples[:max(0, 5 - len(a.examples))])
+        if k == "dp":
+            a.floor_rows += b.floor_rows
+            a.worst_rel = max(a.worst_rel, b.worst_rel)
+
+
+def for_blocks_parallel(par: Parity, R: int, check, chunk_rows=16384, workers=4):
+    """Run check(part, r0, r1, nthreads) over the row blocks [r0, r1) of [0, R) with `workers`
+    blocks in flight at once (device-to-host copies, the oracle and numpy release the GIL); each
+    block has its share of the host's cores for the oracle and its own tallies, merged into par
+    in row order. An exception in a block (an assertion) propagates."""
+    import concurrent.futures as cf
+    nthreads = max(1, oracle.default_threads() // workers)
+
+    def one(r0):
+        part = Parity(par.name)
+        check(part, r0, min(R, r0 + chunk_rows), nthreads)
+        return part
+
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        for part in ex.map(one, range(0, R, chunk_rows)):
+            merge(par, part)
+
+
+def compare_full_parallel(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, chunk_rows=16384,
+                          workers=4):
+    """compare_full over all rows, several blocks at once (for_blocks_parallel)."""
+    def check(part, r0, r1, nthreads):
+        compare_rows(part, x[r0:r1], g[r0:r1], p[r0:r1], out[r0:r1], dx[r0:r1], dp[r0:r1], beta, lbeta,
+                     row0=r0, nthreads=nthreads)
+
+    for_blocks_parallel(par, x.shape[0], check, chunk_rows, workers)
 
 
 def sample_rows(R: int, n_random: int = 2048, edge: int = 64, seed: int = 0) -> torch.Tensor:
