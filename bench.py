@@ -708,6 +708,37 @@ def time_adam(sg, dev, steps, n=1 << 28, chunk=1 << 24, nslots=2, seed=7):
             "timing": "host wall clock per step (the step returns when every chunk's weights are on the device)"}
 
 
+def host_numa_report(h):
+    """Where the pages of host tensor h live (NUMA node -> pages, from /proc/self/numa_maps) and
+    each node's free memory: a slow host link on some boxes goes with buffers placed away from
+    the GPU's node. Best effort (None where the files are missing)."""
+    try:
+        a0, a1 = h.data_ptr(), h.data_ptr() + h.numel() * h.element_size()
+        starts = set()
+        with open("/proc/self/maps") as f:                 # the mappings that overlap h
+            for line in f:
+                lo, hi = (int(v, 16) for v in line.split()[0].split("-"))
+                if lo < a1 and hi > a0:
+                    starts.add(lo)
+        pages = {}
+        with open("/proc/self/numa_maps") as f:
+            for line in f:
+                if int(line.split()[0], 16) in starts:
+                    for w in line.split():
+                        if w.startswith("N") and "=" in w:
+                            k, v = w[1:].split("=")
+                            pages[k] = pages.get(k, 0) + int(v)
+        free = {}
+        import glob
+        for d in sorted(glob.glob("/sys/devices/system/node/node*")):
+            for line in open(d + "/meminfo"):
+                if "MemFree" in line:
+                    free[d.rsplit("node", 1)[1]] = int(line.split()[3]) // (1 << 20)
+        return {"pages_by_node": pages, "node_free_GiB": free}
+    except (OSError, ValueError):
+        return None
+
+
 def pinned_like(t):
     """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size, touched).
 
@@ -821,7 +852,8 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_ro
     t_in = copy_ms(lambda: x.copy_(xh, non_blocking=True))
     t_out = copy_ms(lambda: dxh.copy_(dx, non_blocking=True))
     t_both = copy_ms(both_ways)
-    link = {"h2d_GB_s": nbx / t_in / 1e6, "d2h_GB_s": nbx / t_out / 1e6, "both_ways_GB_s": 2 * nbx / t_both / 1e6}
+    link = {"h2d_GB_s": nbx / t_in / 1e6, "d2h_GB_s": nbx / t_out / 1e6, "both_ways_GB_s": 2 * nbx / t_both / 1e6,
+            "host_memory": host_numa_report(xh)}
     link_ms = (h2d + d2h) / (link["both_ways_GB_s"] * 1e6)
     for t in (xh, gh, ph, oh, dxh, dph):
         unpin(t)
