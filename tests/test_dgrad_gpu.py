@@ -51,6 +51,9 @@ CASES = {
     "three_way_split": ([129, 0, 200], 768, 64),
     "uneven_split": ([300, 77], 1280, 128),
     "large_experts": ([600, 517, 1000], 1024, 128),
+    # either side of the host's choice (experts averaging 512 rows or more: one cluster of 4)
+    "cluster_choice_511": ([510, 512], 1024, 64),
+    "cluster_choice_512": ([512, 512], 1024, 64),
 }
 
 

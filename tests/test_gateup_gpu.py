@@ -84,6 +84,9 @@ CASES = {
     # with odd tile counts (9 and 5: a last unit of one tile), an empty expert and partial tiles
     "two_tile_units": ([1100, 600, 0, 900], 256, 128),
     "two_tile_units_real_widths": ([700, 1300], 3072, 3584),
+    # either side of the host's choice (experts averaging 512 rows or more: two-tile units)
+    "unit_choice_511": ([510, 512], 256, 64),
+    "unit_choice_512": ([512, 512], 256, 64),
 }
 
 
