@@ -436,12 +436,23 @@ def pin_grouped_dgrad(o_mod):
                 ref = sum(dyf[r, d] * wtf[e, j, d] for d in range(D))
                 assert abs(g[r, j] - ref) <= 1e-12 * max(1.0, abs(ref))
     dx, dp, _ = o_mod.dgrad_bwd_router(x, dy, wt, off, p)
-    a = o_mod.fwd_f64(_bits_to_f32(x).astype(np.float64))
+    xf = _bits_to_f32(x).astype(np.float64)
+    a = o_mod.fwd_f64(xf)
     for e in range(E):
         for r in range(off[e], off[e + 1]):
             o_e = wtf[e].T @ a[r]                          # o_e = W_down,e · a_e  (W_down,e = wt[e]ᵀ)
             naive = float(dyf[r] @ o_e)                    # <dL/dy, o_e>
             assert abs(dp[r] - naive) <= 1e-12 * max(1.0, abs(naive))
+            # dx: central differences of p_r·<dL/dy, W_down,e·a_e(x_r)> in each input
+            for k in range(2 * H):
+                hk = 1e-6 * max(1.0, abs(xf[r, k]))
+                xp, xm = xf[r].copy(), xf[r].copy()
+                xp[k] += hk
+                xm[k] -= hk
+                fp = float(dyf[r] @ (wtf[e].T @ o_mod.fwd_f64(xp[None, :])[0]))
+                fm = float(dyf[r] @ (wtf[e].T @ o_mod.fwd_f64(xm[None, :])[0]))
+                fd = float(p[r]) * (fp - fm) / (2 * hk)
+                assert abs(dx[r, k] - fd) <= 1e-6 * max(1.0, abs(fd))
 
 
 # ---------------------------------------------------------------- bf16 rounding, gate/up projection

@@ -120,3 +120,94 @@ def test_planted_mistake_is_caught(tmp_path, name):
     o = oracle.compile_variant(text.replace(find, repl), str(tmp_path / f"{name}.so"))
     failed = failing_pins(o)
     assert failed, f"no pin catches the planted mistake {name}"
+
+
+# ---------------------------------------------------------------- the oracle's numpy parts
+# The expert-grouped projections are numpy code (an fp64 matmul per expert): planted mistakes
+# there replace one oracle function with a wrong one and must trip the GEMM pins.
+
+class Shim:
+    """The oracle module with some of its functions replaced."""
+
+    def __init__(self, **over):
+        self.__dict__.update(over)
+
+    def __getattr__(self, name):
+        return getattr(oracle, name)
+
+
+def _bits_f64(b):
+    return (np.asarray(b).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def _gateup_fwd_from(grouped, rounding="rne", out_from="rounded"):
+    def gateup_fwd(h, w, off, beta=4.0, lbeta=25.0, nthreads=0):
+        x, mag = grouped(h, w, off)
+        if rounding == "rne":
+            xb = oracle.round_bf16_array(x)
+        else:                                   # truncation toward zero
+            xb = (x.astype(np.float32).view(np.uint32) >> 16).astype(np.uint16)
+        src = xb if out_from == "rounded" else None
+        out = oracle.fwd_bf16(src, beta, lbeta) if src is not None else oracle.fwd_f64(x, beta, lbeta)
+        return x, xb, out, mag
+    return gateup_fwd
+
+
+def _swap_halves(grouped):
+    def f(h, w, off):
+        x, mag = grouped(h, w, off)
+        H = x.shape[1] // 2
+        idx = np.r_[H:2 * H, 0:H]
+        return x[:, idx], mag[:, idx]
+    return f
+
+
+def _next_expert_weights_gateup(h, w, off):
+    return oracle.grouped_gateup(h, np.roll(np.asarray(w), -1, axis=0), off)
+
+
+def _dp_times_p(x, dy, wt, off, p, *a, **k):
+    dx, dp, dpa = oracle.dgrad_bwd_router(x, dy, wt, off, p, *a, **k)
+    return dx, dp * np.asarray(p, dtype=np.float64), dpa
+
+
+def _dgrad_without_p_in_dx(x, dy, wt, off, p, *a, **k):
+    return oracle.dgrad_bwd_router(x, dy, wt, off, np.ones_like(np.asarray(p)), *a, **k)
+
+
+NUMPY_MUTANTS = {
+    "dgrad_next_expert_weights": ("dgrad", lambda: Shim(
+        grouped_dgrad=lambda dy, wt, off: oracle.grouped_dgrad(dy, np.roll(np.asarray(wt), -1, axis=0), off))),
+    "dgrad_rows_shifted": ("dgrad", lambda: Shim(
+        grouped_dgrad=lambda dy, wt, off: np.roll(oracle.grouped_dgrad(dy, wt, off), 1, axis=0))),
+    "dgrad_weights_not_transposed": ("dgrad", lambda: Shim(
+        grouped_dgrad=lambda dy, wt, off: oracle.grouped_dgrad(
+            dy, np.ascontiguousarray(np.asarray(wt).reshape(wt.shape[0], -1)[:, :wt.shape[1] * wt.shape[2]]
+                                     .reshape(wt.shape[0], wt.shape[2], wt.shape[1]).transpose(0, 2, 1)), off))),
+    "dgrad_dp_times_p": ("dgrad", lambda: Shim(dgrad_bwd_router=_dp_times_p)),
+    "dgrad_router_weight_ignored": ("dgrad", lambda: Shim(dgrad_bwd_router=_dgrad_without_p_in_dx)),
+    "gateup_halves_swapped": ("gateup", lambda: Shim(
+        grouped_gateup=_swap_halves(oracle.grouped_gateup),
+        gateup_fwd=_gateup_fwd_from(_swap_halves(oracle.grouped_gateup)))),
+    "gateup_next_expert_weights": ("gateup", lambda: Shim(
+        grouped_gateup=_next_expert_weights_gateup, gateup_fwd=_gateup_fwd_from(_next_expert_weights_gateup))),
+    "gateup_truncating_rounding": ("gateup", lambda: Shim(
+        gateup_fwd=_gateup_fwd_from(oracle.grouped_gateup, rounding="trunc"))),
+    "gateup_out_from_unrounded_x": ("gateup", lambda: Shim(
+        gateup_fwd=_gateup_fwd_from(oracle.grouped_gateup, out_from="exact"))),
+}
+
+GEMM_PINS = {"dgrad": _pins.pin_grouped_dgrad, "gateup": _pins.pin_grouped_gateup}
+
+
+def test_numpy_control_passes():
+    for pin in GEMM_PINS.values():
+        pin(Shim())
+    _pins.pin_grouped_gateup(Shim(gateup_fwd=_gateup_fwd_from(oracle.grouped_gateup)))
+
+
+@pytest.mark.parametrize("name", sorted(NUMPY_MUTANTS))
+def test_planted_mistake_in_numpy_part_is_caught(name):
+    which, make = NUMPY_MUTANTS[name]
+    with np.errstate(all="ignore"), pytest.raises((AssertionError, ValueError)):
+        GEMM_PINS[which](make())
