@@ -740,15 +740,23 @@ def host_numa_report(h):
 
 
 def pinned_like(t):
-    """Host tensor of t's shape and dtype, page-locked with cudaHostRegister (exact size, touched).
+    """Host tensor of t's shape and dtype in its own page-aligned anonymous mapping, touched and
+    page-locked with cudaHostRegister (exact size).
 
     Registered portable | mapped (flags 3): on this platform device->host copies into memory
-    registered with flags 0 ran at ~31 GB/s against ~190 GB/s with these flags."""
+    registered with flags 0 ran at ~31 GB/s against ~190 GB/s with these flags. A mapping of its
+    own rather than torch's (malloc'd) host storage: on some boxes of the pool, host->device
+    copies from registered 16 GB malloc'd buffers ran at ~18 GB/s against ~140 GB/s from
+    registered page-aligned mappings of the same size (measured back to back on one box)."""
+    import mmap
+
+    import numpy as np
     import torch
-    h = torch.empty(t.shape, dtype=t.dtype)
-    if h.numel():
-        h.view(-1).view(torch.uint8).zero_()
-    rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), h.numel() * h.element_size(), 3)
+    nbytes = t.numel() * t.element_size()
+    buf = np.frombuffer(mmap.mmap(-1, max(nbytes, 1)), dtype=np.uint8, count=nbytes)
+    buf[:] = 0                                      # touch every page before registering
+    h = torch.from_numpy(buf).view(t.dtype).view(t.shape)   # keeps the mapping alive
+    rc = torch.cuda.cudart().cudaHostRegister(h.data_ptr(), nbytes, 3)
     if int(rc) != 0:
         raise RuntimeError(f"cudaHostRegister failed: {rc}")
     return h
