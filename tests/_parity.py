@@ -146,12 +146,14 @@ def compare_rows(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, row0=0
 
 
 def compare_full(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.0, chunk_rows=8192):
-    R = x.shape[0]
-    for r0 in range(0, R, chunk_rows):
-        r1 = min(R, r0 + chunk_rows)
-        compare_rows(par, x[r0:r1], None if g is None else g[r0:r1], None if p is None else p[r0:r1],
-                     None if out is None else out[r0:r1], None if dx is None else dx[r0:r1],
-                     None if dp is None else dp[r0:r1], beta, lbeta, row0=r0)
+    """Every row, in blocks of chunk_rows (several blocks at once: for_blocks_parallel)."""
+    cut = lambda t, r0, r1: None if t is None else t[r0:r1]
+
+    def check(part, r0, r1, nthreads):
+        compare_rows(part, x[r0:r1], cut(g, r0, r1), cut(p, r0, r1), cut(out, r0, r1), cut(dx, r0, r1),
+                     cut(dp, r0, r1), beta, lbeta, row0=r0, nthreads=nthreads)
+
+    for_blocks_parallel(par, x.shape[0], check, chunk_rows)
 
 
 def merge(into: Parity, part: Parity):

@@ -11,7 +11,7 @@ import pytest
 import torch
 
 import situ_inputs as si
-from _parity import Parity, bits_of, compare_full, compare_full_parallel, sample_rows
+from _parity import Parity, bits_of, compare_full, compare_full_parallel, for_blocks_parallel, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -357,9 +357,11 @@ def check_fp8_rows(par, x, g, p, out, xq, xs, dx, dp, beta=4.0, lbeta=25.0, row0
 
 
 def check_fp8_full(par, x, g, p, out, xq, xs, dx, dp, beta=4.0, lbeta=25.0, chunk_rows=8192):
-    for a in range(0, x.shape[0], chunk_rows):
-        b = min(x.shape[0], a + chunk_rows)
-        check_fp8_rows(par, x[a:b], g[a:b], p[a:b], out[a:b], xq[a:b], xs[a:b], dx[a:b], dp[a:b], beta, lbeta, a)
+    def check(part, a, b, nthreads):
+        check_fp8_rows(part, x[a:b], g[a:b], p[a:b], out[a:b], xq[a:b], xs[a:b], dx[a:b], dp[a:b], beta, lbeta, a,
+                       nthreads)
+
+    for_blocks_parallel(par, x.shape[0], check, chunk_rows)
 
 
 @pytest.mark.parametrize("name", ["routed_r1024_h3072", "saturating_mix_r16384_h3072"])
