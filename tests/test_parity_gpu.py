@@ -433,6 +433,33 @@ def test_fp8_zero_tiny_and_huge_blocks(sg):
     par.assert_ok()
 
 
+def test_fp8_scale_for_every_amax_mantissa(sg):
+    """Block maxima with each of the 128 bf16 mantissas at exponents from 2^-100 to 2^120 (and
+    a zero block): the inverse scales and scales follow the block amax through a mantissa table
+    and a power of two, so every code and scale must still equal the oracle's divisions."""
+    H = 3072                                   # 24 blocks per half, 48 per row
+    R = 128
+    rng = np.random.default_rng(21)
+    x = rng.uniform(-1.0, 1.0, (R, 2 * H)).astype(np.float32)
+    nb = 2 * H // 128
+    for r in range(R):
+        for b in range(nb):
+            f = (r + 37 * b) % 128
+            e = int(rng.integers(-100, 121))
+            amax = np.float32((1.0 + f / 128.0) * 2.0 ** e)     # exactly a bf16 value
+            blk = x[r, b * 128:(b + 1) * 128] * np.float32(0.99) * amax
+            blk[int(rng.integers(0, 128))] = amax if rng.random() < 0.5 else -amax
+            x[r, b * 128:(b + 1) * 128] = blk
+    x[0, :128] = 0.0                            # a zero block: the floor
+    xt = torch.from_numpy(x).to(torch.bfloat16).to(DEV)
+    g = torch.randn(R, H, generator=torch.Generator().manual_seed(22)).to(torch.bfloat16).to(DEV)
+    p = torch.rand(R, generator=torch.Generator().manual_seed(23)).to(DEV)
+    out, xq, xs, dx, dp = run_fp8(sg, xt, g, p)
+    par = Parity("fp8 amax mantissa sweep")
+    check_fp8_full(par, xt, g, p, out, xq, xs, dx, dp)
+    par.assert_ok()
+
+
 def test_fp8_misaligned_codes_take_the_element_path(sg):
     R, H = 9, 1000
     w = si.custom(R, H, seed=3)
