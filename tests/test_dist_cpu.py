@@ -70,3 +70,32 @@ def test_clock_parsing():
     assert c["sm_mhz"] == 1980 and c["sm_max_mhz"] == 2070 and c["samples"] == 3
     assert c["reasons"] == ["sw_power_cap"]
     assert bench.parse_clock_lines([])["samples"] == 0
+
+
+def test_reference_arm_line_keeps_the_contract(monkeypatch, capsys):
+    """--impl reference on rank 0 prints one JSON line with the contract's keys: the oracle timed
+    on the host cores on a bounded sample, its own cpu_baseline and a host-only e2e."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    assert bench.main(["--impl", "reference", "--steps", "2", "--warmup", "1", "--rows", "512"]) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    line = json.loads(lines[0])
+    for key in ("impl", "metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in line, key
+    assert line["impl"] == "reference" and line["value"] > 0 and line["steps"] == 2 and line["warmup"] == 1
+    assert line["config"]["workload"] == bench.WORKLOAD
+    cb = line["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert line["e2e"]["value"] == line["value"] and line["e2e"]["unit"] == line["unit"]
+
+
+def test_host_numa_report_finds_the_buffer():
+    h = torch.empty(1 << 22, dtype=torch.uint8)
+    h.zero_()
+    rep = bench.host_numa_report(h)
+    if rep is not None:                         # /proc and /sys present (Linux)
+        assert sum(rep["pages_by_node"].values()) > 0 and rep["node_free_GiB"]
