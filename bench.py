@@ -41,7 +41,8 @@ NCU_TRAFFIC = {
     "source_sha256": "ec21a529bb2653914f7ae1ff9c89256ff96d1acbfcc0a7aaf928f02d1d13056b",
     "bwd_bytes_per_row": (1.208449e9 + 0.769850368e9) / 65536,
     "fwd_bytes_per_row": (0.805462e9 + 0.3650048e9) / 65536,
-    "capture": "ncu --set full, R=65536 H=3072, scaled by rows (profiles/situ_glu_fwd_bwd_ncu_full_r65536_h3072.md)",
+    "capture": "ncu --set full capture, backward kernel, R=65536, H=3072: dram__bytes_read.sum + "
+               "dram__bytes_write.sum per row, times R; valid for kernel sources of sha256 {sha:.12}",
 }
 
 
@@ -438,7 +439,8 @@ def run_native(args):
                      "peak_source": f"{peak_src} HBM copy bandwidth (MEASURED_PEAKS.json hbm_gbs)"
                      if peak_src == "measured" else "fallback 6.8 TB/s",
                      "algorithmic_bytes_per_launch": bwd_bytes, "traffic": traffic,
-                     "traffic_source": NCU_TRAFFIC["capture"] if traffic is not None else None},
+                     "traffic_source": NCU_TRAFFIC["capture"].format(sha=NCU_TRAFFIC["source_sha256"])
+                     if traffic is not None else None},
         "clocks": clocks,
         "gpu_launches": 2 * K,
         "e2e": e2e,

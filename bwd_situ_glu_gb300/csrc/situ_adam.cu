@@ -276,7 +276,10 @@ int situ_adam_stream_step(const float* grad_dev, void* weight_dev, float* master
             if (e == cudaSuccess) e = cudaEventRecord(ev_d2h[s], stream);
         }
     }
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);         // every chunk's weights are on the device
+    // every chunk's weights are on the device; and on an error, no copy this call queued may still
+    // be reading or writing the caller's staging slots when it returns
+    const cudaError_t es = cudaStreamSynchronize(stream);
+    if (e == cudaSuccess) e = es;
 
     crew.stop.store(true, std::memory_order_release);
     for (auto& th : pool) th.join();

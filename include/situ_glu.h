@@ -277,7 +277,9 @@ int situ_adam_update_host(float* master, void* m, void* v, const float* g, void*
  * (so after the kernels that produced the gradients), gradient chunk c + nslots in flight while
  * chunk c is updated by nthreads host threads; returns when every chunk's weights are on the
  * device. Creates and destroys 2*nslots CUDA events per call; allocates no memory. On a CUDA
- * error (SITU_GLU_CUDA_ERROR) a prefix of the chunks may have been updated. */
+ * error (SITU_GLU_CUDA_ERROR) a prefix of the chunks may have been updated; the call still
+ * waits for `stream` (every copy it queued) before returning, so staging may be reused or
+ * freed as soon as it returns, whatever the status. */
 int situ_adam_stream_step(const float* grad_dev, void* weight_dev, float* master, void* m, void* v,
                           int64_t n, const situ_adam_params* hp, void* staging, int64_t chunk,
                           int nslots, int nthreads, cudaStream_t stream);

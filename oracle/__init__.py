@@ -375,22 +375,6 @@ def dgrad_bwd_router(x_bits, dy_bits, wt_bits, offsets, p, beta: float = 4.0, lb
     return _default().bwd_router_f64(x, g, np.asarray(p, dtype=np.float32).astype(np.float64), beta, lbeta, nthreads)
 
 
-def dgrad_bwd_router_rows(x_bits, dy_bits, experts, wt_of_expert, p, beta: float = 4.0, lbeta: float = 25.0):
-    """The fused op on selected rows only: row i belongs to expert experts[i]; wt_of_expert(e)
-    returns that expert's W_downᵀ as bf16 bits [H, D]. Same arithmetic as dgrad_bwd_router."""
-    dy = (np.ascontiguousarray(dy_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    x = (np.ascontiguousarray(x_bits).view(np.uint16).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
-    experts = np.asarray(experts)
-    H = x.shape[1] // 2
-    g = np.empty((dy.shape[0], H), dtype=np.float64)
-    for e in np.unique(experts):
-        rows = np.nonzero(experts == e)[0]
-        wt = (np.ascontiguousarray(wt_of_expert(int(e))).view(np.uint16).astype(np.uint32) << 16).view(
-            np.float32).astype(np.float64)
-        g[rows] = dy[rows] @ wt.T
-    return _default().bwd_router_f64(x, g, np.asarray(p, dtype=np.float32).astype(np.float64), beta, lbeta)
-
-
 # ---------------------------------------------------------------- fused gate/up projection forward
 
 def round_bf16(v: float) -> int:

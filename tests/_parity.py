@@ -198,14 +198,34 @@ def compare_full_parallel(par: Parity, x, g, p, out, dx, dp, beta=4.0, lbeta=25.
     for_blocks_parallel(par, x.shape[0], check, chunk_rows, workers)
 
 
-def sample_rows(R: int, n_random: int = 2048, edge: int = 64, seed: int = 0) -> torch.Tensor:
-    rng = np.random.default_rng(seed)
-    idx = set(range(min(edge, R))) | set(range(max(0, R - edge), R))
-    idx |= set(rng.integers(0, R, size=min(n_random, R)).tolist())
-    return torch.tensor(sorted(idx), dtype=torch.int64)
+def expert_groups(offsets, rows_per_group: int = 16384):
+    """Split experts 0..E-1 (rows offsets[e]..offsets[e+1]-1, grouped by expert) into runs of
+    consecutive experts holding about rows_per_group rows each: a list of (e0, e1), e1 exclusive."""
+    offsets = np.asarray(offsets, dtype=np.int64)
+    E = len(offsets) - 1
+    groups, e0 = [], 0
+    for e in range(E):
+        if offsets[e + 1] - offsets[e0] >= rows_per_group or e == E - 1:
+            groups.append((e0, e + 1))
+            e0 = e + 1
+    return groups
 
 
-def compare_sampled(par: Parity, x, g, p, out, dx, dp, rows: torch.Tensor, beta=4.0, lbeta=25.0):
-    dev_rows = rows.to(x.device)
-    take = lambda t: None if t is None else t.index_select(0, dev_rows)
-    compare_rows(par, take(x), take(g), take(p), take(out), take(dx), take(dp), beta, lbeta)
+def for_expert_groups_parallel(par: Parity, offsets, check, rows_per_group: int = 16384, workers: int = 4):
+    """Run check(part, e0, e1, nthreads) over runs of consecutive experts (expert_groups) with
+    `workers` runs in flight at once, each with its own tallies merged into par in row order;
+    returns the list of check's return values. An exception in a run propagates."""
+    import concurrent.futures as cf
+    nthreads = max(1, oracle.default_threads() // workers)
+
+    def one(g):
+        part = Parity(par.name)
+        res = check(part, g[0], g[1], nthreads)
+        return part, res
+
+    results = []
+    with cf.ThreadPoolExecutor(max_workers=workers) as ex:
+        for part, res in ex.map(one, expert_groups(offsets, rows_per_group)):
+            merge(par, part)
+            results.append(res)
+    return results

@@ -17,7 +17,7 @@ import torch
 
 import oracle
 import situ_inputs as si
-from _parity import Parity, bf16_bits_to_f64, bits_of, sample_rows
+from _parity import Parity, bf16_bits_to_f64, bits_of, for_expert_groups_parallel
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -136,9 +136,11 @@ def test_gateup_rejects_unsupported_shapes(sg):
 
 
 @pytest.mark.slow
-def test_gateup_expert_grouped_full_size_sampled(sg):
+def test_gateup_expert_grouped_full_size_all_rows(sg):
     """R = 262144 routed rows grouped by expert over 896 experts (16384 tokens x top-16),
-    H = 3072, D = 3584: the full-size launch, checked on sampled rows."""
+    H = 3072, D = 3584: the full-size launch, every row of x and out checked (runs of
+    consecutive experts streamed to the host, the fp64 projections on each run, several runs at
+    once)."""
     wl = si.get("expert_grouped_r262144_h3072")
     _, experts, _ = si.router_rows(wl.tokens, wl.seed, order="expert")
     counts = np.bincount(experts.numpy(), minlength=si.N_EXPERTS)
@@ -150,24 +152,30 @@ def test_gateup_expert_grouped_full_size_sampled(sg):
     w = torch.empty(E, 2 * H, D, dtype=torch.bfloat16, device=DEV)
     for e in range(E):
         w[e] = (torch.randn(2 * H, D, generator=gen, device=DEV) * (wl.x_std / D ** 0.5)).to(torch.bfloat16)
-    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=DEV)
+    off_np = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    off = torch.from_numpy(off_np).to(DEV)
     status = torch.zeros(1, dtype=torch.int32, device=DEV)
     x, out = sg.situ_glu_fwd_gateup(h, w, off, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) == 0
-    assert bool(torch.isfinite(x).all()) and bool(torch.isfinite(out).all())
-    rows = sample_rows(wl.R, n_random=512, seed=12).to(DEV)
-    row_expert = torch.bucketize(rows, off[1:], right=True).cpu().numpy()
-    rows_np = rows.cpu().numpy()
-    xg, og = bits_of(x.index_select(0, rows)), bits_of(out.index_select(0, rows))
-    differs = 0
-    for e in np.unique(row_expert):
-        sel = np.nonzero(row_expert == e)[0]
-        hb = bits_of(h.index_select(0, torch.from_numpy(rows_np[sel]).to(DEV)))
-        x_exact, xb_ref, _, mag = oracle.gateup_fwd(hb, bits_of(w[e]).reshape(1, 2 * H, D),
-                                                    np.array([0, len(sel)], dtype=np.int64))
-        differs += check(f"gateup expert_grouped_r262144 expert {e}", xg[sel], og[sel], x_exact, xb_ref, mag)
-    assert differs <= max(8, xg.size // 200)
+
+    def run_group(part, e0, e1, nthreads):
+        r0, r1 = int(off_np[e0]), int(off_np[e1])
+        if r1 == r0:
+            return 0, 0
+        x_exact, xb_ref, _, mag = oracle.gateup_fwd(bits_of(h[r0:r1]), bits_of(w[e0:e1]).reshape(e1 - e0, 2 * H, D),
+                                                    off_np[e0:e1 + 1] - r0, nthreads=nthreads)
+        xg = bits_of(x[r0:r1])
+        differs = check(f"gateup expert_grouped_r262144 experts {e0}..{e1 - 1}", xg, bits_of(out[r0:r1]), x_exact,
+                        xb_ref, mag)
+        return differs, xg.size
+
+    par = Parity("gateup expert_grouped_r262144 (all rows)")
+    res = for_expert_groups_parallel(par, off_np, run_group, rows_per_group=2048)
+    differs, n = sum(r[0] for r in res), sum(r[1] for r in res)
+    assert n == wl.R * 2 * H
+    assert differs <= max(8, n // 200)
+    print(f"gateup expert_grouped_r262144: every row checked, {n} x elements, {differs} differ from RNE(exact)")
     del h, w, x, out
     torch.cuda.empty_cache()
 

@@ -25,13 +25,21 @@ def _claims():
     return out
 
 
-def _naive_forward(x: torch.Tensor, beta: float = 4.0, lbeta: float = 25.0) -> torch.Tensor:
-    # the definition as plain PyTorch ops in fp32 (same op sequence as the naive version:
-    # widen, split in halves, tanh/sigmoid gate, tanh linear, product, narrow)
-    gate, lin = torch.chunk(x.float(), 2, dim=-1)
-    gate = beta * torch.tanh(gate / beta) * torch.sigmoid(gate)
-    lin = lbeta * torch.tanh(lin / lbeta)
-    return (gate * lin).to(x.dtype)
+def _autograd_graph_of_definition(x: torch.Tensor, beta: float = 4.0, lbeta: float = 25.0) -> torch.Tensor:
+    """SiTU-GLU assembled from the named quantities of the definition (u = x[:, :H],
+    v = x[:, H:]; T, S, G, W, L, a) as plain fp32 autograd ops, so that autograd records what
+    an op-by-op evaluation keeps for the backward: the outputs of tanh and sigmoid, and both
+    factors of every product of two tensors (a product with a scalar keeps nothing)."""
+    H = x.shape[-1] // 2
+    xf = x.float()
+    u, v = xf[:, :H], xf[:, H:]
+    T = torch.tanh(u / beta)          # keeps T
+    S = torch.sigmoid(u)              # keeps S
+    G = (beta * T) * S                # keeps beta*T and S
+    W = torch.tanh(v / lbeta)         # keeps W
+    L = lbeta * W
+    a = G * L                         # keeps G and L
+    return a.to(x.dtype)
 
 
 def test_naive_autograd_keeps_six_fp32_rh_tensors():
@@ -44,7 +52,7 @@ def test_naive_autograd_keeps_six_fp32_rh_tensors():
         return t
 
     with torch.autograd.graph.saved_tensors_hooks(pack, lambda t: t):
-        y = _naive_forward(x)
+        y = _autograd_graph_of_definition(x)
     y.float().sum().backward()
     distinct = {t.data_ptr() for t in packed if t.dtype == torch.float32 and tuple(t.shape) == (R, H)}
     claims = _claims()
