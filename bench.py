@@ -71,6 +71,9 @@ def parse_args(argv=None):
     ap.add_argument("--only-dgrad", action="store_true", help="time only the fused dgrad GEMM (profiling runs)")
     ap.add_argument("--only-gateup", action="store_true", help="time only the fused gate/up GEMM (profiling runs)")
     ap.add_argument("--only-adam", action="store_true", help="time only the streamed host Adam step")
+    ap.add_argument("--unfused", action="store_true",
+                    help="with --only-dgrad / --only-gateup: also time the unfused route (library GEMM, then the "
+                         "elementwise kernel)")
     ap.add_argument("--adam-params", type=int, default=1 << 28, help="parameters of the Adam leg")
     ap.add_argument("--gemm-rows", type=int, default=None, help="rows split evenly over --gemm-experts")
     ap.add_argument("--gemm-experts", type=int, default=None)
@@ -290,11 +293,11 @@ def run_gemm_only(args):
     line, ok = {}, True
     if args.only_dgrad:
         line["dgrad_fused"] = time_dgrad(sg, dev, args.steps, args.warmup, peak, rows=args.gemm_rows,
-                                         experts=args.gemm_experts)
+                                         experts=args.gemm_experts, unfused=args.unfused)
         ok &= line["dgrad_fused"]["status"] == 0
     if args.only_gateup:
         line["gateup_fused"] = time_gateup(sg, dev, args.steps, args.warmup, peak, rows=args.gemm_rows,
-                                           experts=args.gemm_experts)
+                                           experts=args.gemm_experts, unfused=args.unfused)
         ok &= line["gateup_fused"]["status"] == 0
     if args.only_adam:
         line["adam_stream"] = time_adam(sg, dev, args.steps, n=args.adam_params)
@@ -382,8 +385,8 @@ def run_native(args):
     step_gbs = (fwd_bytes + bwd_bytes) / (elapsed_ms / K * 1e-3) / 1e9
 
     fp8 = None if args.no_fp8 else time_fp8(sg, x, g, p, out, dx, dp, R, H, stream, dev, K, args.warmup, peak)
-    dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak)
-    gateup = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak)
+    dgrad = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak, unfused=True)
+    gateup = None if args.no_gateup else time_gateup(sg, dev, max(3, min(K, 20)), args.warmup, peak, unfused=True)
     # the same kernels on few large experts (32 x 8192 rows: the tensor-bound regime)
     dgrad_large = None if args.no_dgrad else time_dgrad(sg, dev, max(3, min(K, 20)), args.warmup, peak,
                                                         rows=1 << 18, experts=32)
@@ -569,9 +572,43 @@ def gemm_result(workload, ms, flops, nbytes, hbm_peak, steps, status):
             "roofline_frac": max(t_flop, t_byte) / ms, "status": status, "gpu_launches": steps}
 
 
-def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, experts=None):
+def library_grouped_gemm(a, b_kn, off_cpu, out):
+    """The route a fusion replaces starts with a plain library grouped GEMM: out rows of expert e
+    = a[rows of e] @ b_kn[e] in bf16 (fp32 accumulation), b_kn [E, K, N] (a transposed view of the
+    K-major weights): cuBLAS per expert (torch.mm into row slices of out), captured once into a
+    CUDA graph and replayed, so that launch overhead does not count against it. Returns fn() -> out.
+    (torch's one-launch grouped GEMM is not used: on this GPU it faulted on row counts that are not
+    multiples of 16.)"""
+    import torch
+    E = b_kn.shape[0]
+
+    def per_expert():
+        for e in range(E):
+            r0, r1 = int(off_cpu[e]), int(off_cpu[e + 1])
+            if r1 > r0:
+                torch.mm(a[r0:r1], b_kn[e], out=out[r0:r1])
+
+    side = torch.cuda.Stream(a.device)
+    side.wait_stream(torch.cuda.current_stream(a.device))
+    with torch.cuda.stream(side):
+        per_expert()                                  # cuBLAS handles and workspaces before capture
+    torch.cuda.current_stream(a.device).wait_stream(side)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        per_expert()
+
+    def replay():
+        graph.replay()
+        return out
+    return replay
+
+
+def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, experts=None, unfused=False):
     """Fused down-projection dgrad (tcgen05 grouped GEMM) + backward + router gradient on the
-    expert-grouped workload, D = 3584 (the expert output width), synthetic N(0, 1/D) weights."""
+    expert-grouped workload, D = 3584 (the expert output width), synthetic N(0, 1/D) weights.
+    unfused: also time, on the same tensors, the route the fusion replaces (a library grouped
+    GEMM writing g in bf16, then situ_glu_bwd_router reading it back)."""
     import numpy as np
     import torch
     counts, p, workload, H, x_std = grouped_workload(seed, rows, experts)
@@ -580,7 +617,8 @@ def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, expe
     x = randn_bf16((R, 2 * H), gen, dev, x_std)
     dy = randn_bf16((R, D), gen, dev)
     wt = randn_bf16((E, H, D), gen, dev, 1.0 / D ** 0.5)
-    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=dev)
+    off_cpu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    off = torch.from_numpy(off_cpu).to(dev)
     p = p.to(dev)
     dx = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
     dp = torch.empty(R, dtype=torch.float32, device=dev)
@@ -590,14 +628,32 @@ def time_dgrad(sg, dev, steps, warmup, hbm_peak, seed=5, D=3584, rows=None, expe
                        stream, steps, warmup)
     nbytes = R * D * 2 + E * H * D * 2 + R * 4 * H + R * 4 * H + R * 8 + (E + 1) * 8
     res = gemm_result(f"{workload} x D={D}", ms, 2.0 * R * D * H, nbytes, hbm_peak, steps, int(status.item()))
+    if unfused:
+        g = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
+        gemm = library_grouped_gemm(dy, wt.transpose(1, 2), off_cpu, g)
+        route = "cuBLAS per expert (torch.mm), one CUDA graph"
+        dx2 = torch.empty_like(dx)
+        dp2 = torch.empty_like(dp)
+
+        def unfused_step():
+            sg.situ_glu_bwd_router(x, gemm(), p, dx2, dp2)
+        ms_u = time_launches(unfused_step, stream, steps, warmup)
+        rel = ((dp2 - dp).abs() / dp.abs().clamp_min(1e-30)).median().item()
+        res["unfused"] = {"ms": ms_u, "route": route + ", then situ_glu_bwd_router",
+                          "bytes": nbytes + R * H * 2 * 2, "fused_speedup": ms_u / ms,
+                          "dp_median_rel_diff_vs_fused": rel,
+                          "what": "g = dY·W_down,e written to HBM in bf16 and read back by the backward"}
+        del dx2, dp2, g, gemm
     del x, dy, wt, dx, dp
     torch.cuda.empty_cache()
     return res
 
 
-def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, experts=None):
+def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, experts=None, unfused=False):
     """Fused gate/up projection (tcgen05 grouped GEMM, N = 2H) + SiTU-GLU forward on the
-    expert-grouped workload: h [R, D] ~ N(0, 1), [W_gate; W_up] ~ N(0, x_std²/D) per expert."""
+    expert-grouped workload: h [R, D] ~ N(0, 1), [W_gate; W_up] ~ N(0, x_std²/D) per expert.
+    unfused: also time, on the same tensors, the route the fusion replaces (a library grouped
+    GEMM writing x in bf16, then situ_glu_fwd reading it back)."""
     import numpy as np
     import torch
     counts, _, workload, H, x_std = grouped_workload(seed, rows, experts)
@@ -605,7 +661,8 @@ def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, exp
     gen = torch.Generator(device=dev).manual_seed(seed)
     h = randn_bf16((R, D), gen, dev)
     w = randn_bf16((E, 2 * H, D), gen, dev, x_std / D ** 0.5)
-    off = torch.tensor(np.concatenate([[0], np.cumsum(counts)]), dtype=torch.int64, device=dev)
+    off_cpu = np.concatenate([[0], np.cumsum(counts)]).astype(np.int64)
+    off = torch.from_numpy(off_cpu).to(dev)
     x = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
     out = torch.empty(R, H, dtype=torch.bfloat16, device=dev)
     status = torch.zeros(1, dtype=torch.int32, device=dev)
@@ -613,6 +670,21 @@ def time_gateup(sg, dev, steps, warmup, hbm_peak, seed=6, D=3584, rows=None, exp
     ms = time_launches(lambda: sg.situ_glu_fwd_gateup(h, w, off, x, out, status=status), stream, steps, warmup)
     nbytes = R * D * 2 + E * 2 * H * D * 2 + R * 4 * H + R * 2 * H + (E + 1) * 8
     res = gemm_result(f"{workload} x D={D}", ms, 2.0 * R * D * 2 * H, nbytes, hbm_peak, steps, int(status.item()))
+    if unfused:
+        xu = torch.empty(R, 2 * H, dtype=torch.bfloat16, device=dev)
+        gemm = library_grouped_gemm(h, w.transpose(1, 2), off_cpu, xu)
+        route = "cuBLAS per expert (torch.mm), one CUDA graph"
+        out2 = torch.empty_like(out)
+
+        def unfused_step():
+            sg.situ_glu_fwd(gemm(), out2)
+        ms_u = time_launches(unfused_step, stream, steps, warmup)
+        same = (out2.view(torch.int16) == out.view(torch.int16)).float().mean().item()
+        res["unfused"] = {"ms": ms_u, "route": route + ", then situ_glu_fwd",
+                          "bytes": nbytes + R * 2 * H * 2, "fused_speedup": ms_u / ms,
+                          "out_bitwise_equal_fraction_vs_fused": same,
+                          "what": "the projection x written to HBM in bf16 and read back by the forward"}
+        del out2, xu, gemm
     del h, w, x, out
     torch.cuda.empty_cache()
     return res

@@ -268,12 +268,54 @@ __device__ __forceinline__ Codes16 ld_codes16(const Codes16* p) {
     return v;
 }
 
+// One 16-element chunk of the wide path: codes of both halves, g, the chunk's two block scales.
+// PAIRED (β == 4 only): the two elements of each word through the paired fp32 math (bwd_b4_t2).
+template <bool BETA4, bool PAIRED>
+__device__ __forceinline__ void fp8_chunk(const Codes16& qgv, const Codes16& qlv, const Vec<8>& yv, float scg,
+                                          float scl, float pr, const Coef& c, float2& acc2, Vec<8>& dgo,
+                                          Vec<8>& dlo) {
+    const float kg = scg * c.k_tu, kl = scl * c.k_tv;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint16_t cgi = (uint16_t)(qgv.w[i >> 1] >> (16 * (i & 1)));
+        const uint16_t cli = (uint16_t)(qlv.w[i >> 1] >> (16 * (i & 1)));
+        float u0, u1, v0, v1;
+        e4m3x2_to_f32(cgi, u0, u1);
+        e4m3x2_to_f32(cli, v0, v1);
+        const float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
+        if constexpr (BETA4 && PAIRED) {
+            const float2 gg = situ::pair(g0, g1);
+            const situ::Bwd2 b = situ::bwd_b4_t2(situ::pair(fabsf(u0) * kg, fabsf(u1) * kg),
+                                                 situ::pair(fabsf(v0) * kl, fabsf(v1) * kl), sign_of(u0), sign_of(u1),
+                                                 sign_of(v0), sign_of(v1), __fmul2_rn(situ::pair(pr, pr), gg), c);
+            acc2 = __ffma2_rn(gg, b.a16, acc2);
+            dgo.w[i] = pack_bf16x2(b.dgate.x, b.dgate.y);
+            dlo.w[i] = pack_bf16x2(b.dlin.x, b.dlin.y);
+        } else {
+            situ::Bwd b0, b1;
+            if constexpr (BETA4) {
+                b0 = situ::bwd_b4_t(fabsf(u0) * kg, fabsf(v0) * kl, sign_of(u0), sign_of(v0), pr * g0, c);
+                b1 = situ::bwd_b4_t(fabsf(u1) * kg, fabsf(v1) * kl, sign_of(u1), sign_of(v1), pr * g1, c);
+            } else {
+                b0 = situ::bwd_gen(__fmul_rn(u0, scg), __fmul_rn(v0, scl), pr * g0, c);
+                b1 = situ::bwd_gen(__fmul_rn(u1, scg), __fmul_rn(v1, scl), pr * g1, c);
+            }
+            acc2.x = fmaf(g0, b0.a16, acc2.x);
+            acc2.y = fmaf(g1, b1.a16, acc2.y);
+            dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
+            dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
+        }
+    }
+}
+
 // Wide path: H % 16 == 0; xq 16-byte, g and dx 32-byte aligned. A lane takes 16 elements per
-// step (16 bytes of codes per half, 32 bytes of g); a warp step covers four scale blocks, one per
-// group of 8 lanes. For beta = 4 the dequantisation scale folds into the exponent arguments:
-// u enters the backward only through |u|·k_tu and its sign, so t = |value(code)|·(scale·k_tu)
-// replaces value·scale followed by |·|·k_tu (one fp32 rounding less than the oracle's two).
-template <bool BETA4, int TPB>
+// chunk (16 bytes of codes per half, 32 bytes of g) and loads U chunks before any math; a warp
+// chunk covers four scale blocks, one per group of 8 lanes. For beta = 4 the dequantisation
+// scale folds into the exponent arguments: u enters the backward only through |u|·k_tu and its
+// sign, so t = |value(code)|·(scale·k_tu) replaces value·scale followed by |·|·k_tu (one fp32
+// rounding less than the oracle's two). The FP8 row moves fewer bytes per element than the bf16
+// one, so the loads in flight per thread (U·64 bytes) set the bandwidth more than the arithmetic.
+template <bool BETA4, int TPB, int U, bool PAIRED>
 __global__ void __launch_bounds__(TPB, 1) bwd_fp8_wide_kernel(const Codes16* __restrict__ xq,
                                                               const float* __restrict__ xs,
                                                               const Vec<8>* __restrict__ g,
@@ -292,41 +334,34 @@ __global__ void __launch_bounds__(TPB, 1) bwd_fp8_wide_kernel(const Codes16* __r
         Vec<8>* dgr = dx + r * (2 * (int64_t)cpr);
         Vec<8>* dlr = dgr + cpr;
         const float pr = 16.0f * p[r];   // 16·p: see situ::Bwd
-        float acc = 0.0f;
-        for (int c0 = 0; c0 < cpr; c0 += 32) {
-            const int ci = c0 + lane;
-            if (ci < cpr) {
-                const Codes16 qgv = ld_codes16(qg + ci), qlv = ld_codes16(ql + ci);
-                const Vec<8> yv = ld_stream<8, true, true>(gr + ci);
-                const float scg = sg[ci >> 3], scl = sl[ci >> 3];
-                const float kg = scg * c.k_tu, kl = scl * c.k_tv;
-                Vec<8> dgo, dlo;
+        float2 acc2 = situ::pair(0.0f, 0.0f);   // the even and the odd elements' sums
+        for (int c0 = 0; c0 < cpr; c0 += 32 * U) {
+            Codes16 qgv[U], qlv[U];
+            Vec<8> yv[U];
+            float scg[U], scl[U];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint16_t cgi = (uint16_t)(qgv.w[i >> 1] >> (16 * (i & 1)));
-                    const uint16_t cli = (uint16_t)(qlv.w[i >> 1] >> (16 * (i & 1)));
-                    float u0, u1, v0, v1;
-                    e4m3x2_to_f32(cgi, u0, u1);
-                    e4m3x2_to_f32(cli, v0, v1);
-                    const float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
-                    situ::Bwd b0, b1;
-                    if constexpr (BETA4) {
-                        b0 = situ::bwd_b4_t(fabsf(u0) * kg, fabsf(v0) * kl, sign_of(u0), sign_of(v0), pr * g0, c);
-                        b1 = situ::bwd_b4_t(fabsf(u1) * kg, fabsf(v1) * kl, sign_of(u1), sign_of(v1), pr * g1, c);
-                    } else {
-                        b0 = situ::bwd_gen(__fmul_rn(u0, scg), __fmul_rn(v0, scl), pr * g0, c);
-                        b1 = situ::bwd_gen(__fmul_rn(u1, scg), __fmul_rn(v1, scl), pr * g1, c);
-                    }
-                    acc = fmaf(g0, b0.a16, acc);
-                    acc = fmaf(g1, b1.a16, acc);
-                    dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
-                    dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
+            for (int k = 0; k < U; ++k) {
+                const int ci = c0 + k * 32 + lane;
+                if (ci < cpr) {
+                    qgv[k] = ld_codes16(qg + ci);
+                    qlv[k] = ld_codes16(ql + ci);
+                    yv[k] = ld_stream<8, true, true>(gr + ci);
+                    scg[k] = sg[ci >> 3];
+                    scl[k] = sl[ci >> 3];
                 }
-                st_stream<8>(dgr + ci, dgo);
-                st_stream<8>(dlr + ci, dlo);
+            }
+#pragma unroll
+            for (int k = 0; k < U; ++k) {
+                const int ci = c0 + k * 32 + lane;
+                if (ci < cpr) {
+                    Vec<8> dgo, dlo;
+                    fp8_chunk<BETA4, PAIRED>(qgv[k], qlv[k], yv[k], scg[k], scl[k], pr, c, acc2, dgo, dlo);
+                    st_stream<8>(dgr + ci, dgo);
+                    st_stream<8>(dlr + ci, dlo);
+                }
             }
         }
-        acc = warp_sum(acc);
+        const float acc = warp_sum(acc2.x + acc2.y);
         if (lane == 0) dp[r] = 16.0f * acc;
     }
 }
@@ -368,6 +403,14 @@ __global__ void __launch_bounds__(kElemThreads) bwd_fp8_elem_kernel(const uint8_
 
 constexpr int kFp8U = 2;
 constexpr int kFp8Tpb = 1024;
+// Launch shape of the wide backward: threads per CTA, chunks per lane, paired fp32 math. Measured at
+// R = 1.6M, H = 3072 (median of 5 x 10 launches, same call): 1024 threads x 1 chunk 7.25 ms
+// (scalar) / 7.27 (paired); 768 x 2 7.32 / 6.86; 512 x 2 8.20 / 7.16; 512 x 3 7.96 / 6.97;
+// 1024 x 2 7.65 / 7.33; 384 x 4 paired 7.75; 640 x 2 paired 6.79 ms. The row moves fewer bytes per
+// element than the bf16 one, so more loads in flight per thread pay, and the paired math frees the
+// issue slots they need.
+constexpr int kWideTpb = 640, kWideU = 2;
+constexpr bool kWidePaired = true;
 
 }  // namespace
 
@@ -427,10 +470,10 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
         const Vec<8>* gv = (const Vec<8>*)g;
         Vec<8>* dxv = (Vec<8>*)dx;
         if (b4)
-            return launch(bwd_fp8_wide_kernel<true, kFp8Tpb>, kFp8Tpb, R, stream, qv, xs, gv, p, dxv, dp, R, cpr,
-                          (int)nb, c);
-        return launch(bwd_fp8_wide_kernel<false, kFp8Tpb>, kFp8Tpb, R, stream, qv, xs, gv, p, dxv, dp, R, cpr,
-                      (int)nb, c);
+            return launch(bwd_fp8_wide_kernel<true, kWideTpb, kWideU, kWidePaired>, kWideTpb, R, stream, qv, xs, gv, p,
+                          dxv, dp, R, cpr, (int)nb, c);
+        return launch(bwd_fp8_wide_kernel<false, kWideTpb, kWideU, false>, kWideTpb, R, stream, qv, xs, gv, p, dxv,
+                      dp, R, cpr, (int)nb, c);
     }
     if (H % 8 == 0 && aligned(xq, 8) && aligned(g, 16) && aligned(dx, 16)) {
         const int cpr = (int)(H / 8);
