@@ -48,3 +48,46 @@ def test_dp_tolerance_and_nan():
     # 0.9e-3 relative passes; 1.1e-3 fails; 0.9e-4 against a cancelled row sum of 100 passes
     # through the 1e-6 * sum|g a| term; NaN on both sides passes
     assert par.t["dp"].bad == 1 and par.t["dp"].floor_rows == 1
+
+
+def test_expert_groups_partition_every_expert_in_order():
+    from _parity import expert_groups
+    rng = np.random.default_rng(3)
+    counts = rng.integers(0, 400, size=97)
+    counts[[0, 5, 96]] = 0                                   # empty experts at the ends and inside
+    off = np.concatenate([[0], np.cumsum(counts)])
+    groups = expert_groups(off, rows_per_group=1000)
+    assert groups[0][0] == 0 and groups[-1][1] == len(counts)
+    assert all(a[1] == b[0] and a[0] < a[1] for a, b in zip(groups, groups[1:]))
+    for e0, e1 in groups[:-1]:                               # every run but the last is full
+        assert off[e1] - off[e0] >= 1000
+        assert off[e1 - 1] - off[e0] < 1000                  # and the shortest run that is
+
+
+def test_expert_groups_parallel_merges_like_one_pass():
+    """Tallies of runs of experts checked several at once equal one pass over all rows."""
+    import torch
+
+    from _parity import Parity, for_expert_groups_parallel
+    rng = np.random.default_rng(4)
+    counts = rng.integers(0, 50, size=40)
+    off = np.concatenate([[0], np.cumsum(counts)])
+    R = int(off[-1])
+    ref = rng.standard_normal((R, 8))
+    gpu = ref + rng.standard_normal((R, 8)) * 1e-4
+    gpu[7, 3] += 1.0                                          # one element out of tolerance
+    bits = torch.from_numpy(gpu).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
+    def check(part, e0, e1, nthreads):
+        a, b = int(off[e0]), int(off[e1])
+        part.bf16("dx", bits[a:b], ref[a:b], row0=a)
+        return b - a
+
+    whole = Parity("one pass")
+    whole.bf16("dx", bits, ref)
+    runs = Parity("runs")
+    rows = for_expert_groups_parallel(runs, off, check, rows_per_group=100, workers=3)
+    assert sum(rows) == R
+    w, r = whole.t["dx"], runs.t["dx"]
+    assert (r.n, r.bad, r.worst_ratio, r.worst_abs) == (w.n, w.bad, w.worst_ratio, w.worst_abs)
+    assert r.bad == 1 and r.examples[0][:2] == (7, 3)
