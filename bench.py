@@ -61,6 +61,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=5)
+    ap.add_argument("--e2e-host", default="mapped", choices=["mapped", "cuda"],
+                    help="host buffers of the e2e leg: page-aligned mappings registered with cudaHostRegister "
+                         "(mapped) or page-locked memory from cudaHostAlloc (cuda)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -401,7 +404,7 @@ def run_native(args):
     # ---------------- end to end through the public API: pinned host in, pinned host out
     e2e = None
     if not args.no_e2e:
-        e2e = time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, args.e2e_steps, world)
+        e2e = time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, args.e2e_steps, world, host=args.e2e_host)
 
     # ---------------- CPU baseline: the oracle on a bounded sample (rank 0 at N = 1 only)
     cpu = None
@@ -845,7 +848,16 @@ def unpin(h):
     torch.cuda.cudart().cudaHostUnregister(h.data_ptr())
 
 
-def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_rows=65536):
+def pinned_cuda(t):
+    """Host tensor of t's shape and dtype in page-locked memory from cudaHostAlloc (torch's pinned
+    allocator), zero-filled."""
+    import torch
+    h = torch.empty(t.shape, dtype=t.dtype, pin_memory=True)
+    h.zero_()
+    return h
+
+
+def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_rows=65536, host="mapped"):
     """The step through the public binding with every input copied in from page-locked host
     memory and every result copied back, inside the timed region.
 
@@ -854,7 +866,8 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_ro
     of chunk i. Events order the reuse of each chunk's device rows across steps."""
     import torch
     steps = max(1, steps)
-    xh, gh, ph, oh, dxh, dph = (pinned_like(t) for t in (x, g, p, out, dx, dp))
+    alloc = pinned_like if host == "mapped" else pinned_cuda
+    xh, gh, ph, oh, dxh, dph = (alloc(t) for t in (x, g, p, out, dx, dp))
     xh.copy_(x)
     gh.copy_(g)
     ph.copy_(p)
@@ -941,12 +954,14 @@ def time_e2e(sg, x, g, p, out, dx, dp, R, H, stream, dev, steps, world, chunk_ro
     link = {"h2d_GB_s": nbx / t_in / 1e6, "d2h_GB_s": nbx / t_out / 1e6, "both_ways_GB_s": 2 * nbx / t_both / 1e6,
             "host_memory": host_numa_report(xh)}
     link_ms = (h2d + d2h) / (link["both_ways_GB_s"] * 1e6)
-    for t in (xh, gh, ph, oh, dxh, dph):
-        unpin(t)
+    if host == "mapped":
+        for t in (xh, gh, ph, oh, dxh, dph):
+            unpin(t)
     return {"value": whole_job_rate(R, world, steps, ms * 1e-3), "unit": "rows/s", "steps": steps,
             "ms_per_step": ms / steps, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "gpu_launches": launches[0],
             "host_link": link, "link_bound_ms_per_step": link_ms, "frac_of_link_bound": link_ms / (ms / steps),
+            "host_buffers": "page-aligned mappings + cudaHostRegister" if host == "mapped" else "cudaHostAlloc",
             "how": f"page-locked host x,g,p -> device -> fwd + bwd via the binding -> out,dx,dp -> host, "
                    f"streamed over {n} row chunks of {chunk_rows} on 3 CUDA streams; host_link measured on "
                    f"the same buffers in the same run"}
