@@ -212,6 +212,22 @@ __device__ __forceinline__ Bwd2 bwd_b4_t2(float2 tg, float2 tl, uint32_t su0, ui
     return o;
 }
 
+// fwd_b4 on two elements (u0, v0) and (u1, v1) with paired fp32 instructions; each lane returns
+// exactly what fwd_b4 returns for it (the same operations in the same order, each rounded as the
+// scalar one).
+__device__ __forceinline__ float2 fwd_b4_2(float u0, float u1, float v0, float v1, const Coef& c) {
+    const float2 one = pair(1.0f, 1.0f);
+    const float2 E = pair(ex2(fabsf(u0) * c.k_tu), ex2(fabsf(u1) * c.k_tu));
+    const float2 e = pair(ex2(fabsf(v0) * c.k_tv), ex2(fabsf(v1) * c.k_tv));
+    const float2 E2 = __fmul2_rn(E, E);
+    const float2 den = __fmul2_rn(__fmul2_rn(__fadd2_rn(one, E), __fadd2_rn(one, E2)), __fadd2_rn(one, e));
+    const float2 r = pair(rcp(den.x), rcp(den.y));
+    const float2 s = pair((u0 < 0.0f) ? E2.x : 1.0f, (u1 < 0.0f) ? E2.y : 1.0f);
+    const float2 omE = __fadd2_rn(one, pair(-E.x, -E.y)), ome = __fadd2_rn(one, pair(-e.x, -e.y));
+    const float2 m = __fmul2_rn(__fmul2_rn(__fmul2_rn(__fmul2_rn(omE, ome), s), r), pair(c.beta_lbeta, c.beta_lbeta));
+    return pair(with_sign(m.x, sign_of(u0) ^ sign_of(v0)), with_sign(m.y, sign_of(u1) ^ sign_of(v1)));
+}
+
 // β == 4. 2 ex2 + 2 rcp.
 __device__ __forceinline__ Bwd bwd_b4(float u, float v, float pg16, const Coef& c) {
     return bwd_b4_t(fabsf(u) * c.k_tu, fabsf(v) * c.k_tv, sign_of(u), sign_of(v), pg16, c);
