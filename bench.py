@@ -38,8 +38,8 @@ FALLBACK_HBM_GBS = 6800.0
 # dram__bytes_write.sum), per row, and the hash of the kernel source it was taken on.
 # Reported only while the source is unchanged; otherwise null.
 NCU_TRAFFIC = {
-    "source_sha256": "6d94d6deb1e88243facdf581ac1d2134fdcf245a6d5ce9718fe1f15dee97cc63",
-    "bwd_bytes_per_row": (1.208387e9 + 0.767566592e9) / 65536,
+    "source_sha256": "fa1328fb9fc97cf3f5b90d940a718f95065ef6fb516ba234eb3595fb94041587",
+    "bwd_bytes_per_row": (1.208397e9 + 0.767695104e9) / 65536,
     "fwd_bytes_per_row": (0.805462e9 + 0.3650048e9) / 65536,
     "capture": "ncu --set full capture, backward kernel, R=65536, H=3072: dram__bytes_read.sum + "
                "dram__bytes_write.sum per row, times R; valid for kernel sources of sha256 {sha:.12}",

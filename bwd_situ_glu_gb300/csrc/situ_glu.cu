@@ -104,33 +104,19 @@ __global__ void __launch_bounds__(kElemThreads) fwd_elem_kernel(const uint16_t* 
 // backward + router-gradient kernels
 // ---------------------------------------------------------------------------
 
-// One chunk: NW words of gate, linear and g -> dgate, dlinear; accumulates g·a into acc (the
-// even elements' sum in x, the odd elements' in y). PAIRED (β == 4): the two elements of each
-// word through the paired fp32 math (situ::bwd_b4_t2), the same values in fewer instructions.
-template <bool BETA4, int NW, bool PAIRED>
+// One chunk: NW words of gate, linear and g -> dgate, dlinear; accumulates g·a into acc.
+template <bool BETA4, int NW>
 __device__ __forceinline__ void bwd_chunk(const Vec<NW>& gv, const Vec<NW>& lv, const Vec<NW>& yv, float p,
-                                          const Coef& c, float2& acc, Vec<NW>& dgo, Vec<NW>& dlo) {
+                                          const Coef& c, float& acc, Vec<NW>& dgo, Vec<NW>& dlo) {
 #pragma unroll
     for (int i = 0; i < NW; ++i) {
-        const float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
-        if constexpr (BETA4 && PAIRED) {
-            const float u0 = bf16_lo(gv.w[i]), u1 = bf16_hi(gv.w[i]), v0 = bf16_lo(lv.w[i]), v1 = bf16_hi(lv.w[i]);
-            const float2 gg = situ::pair(g0, g1);
-            const situ::Bwd2 b = situ::bwd_b4_t2(situ::pair(fabsf(u0) * c.k_tu, fabsf(u1) * c.k_tu),
-                                                 situ::pair(fabsf(v0) * c.k_tv, fabsf(v1) * c.k_tv), sign_of(u0),
-                                                 sign_of(u1), sign_of(v0), sign_of(v1),
-                                                 __fmul2_rn(situ::pair(p, p), gg), c);
-            acc = __ffma2_rn(gg, b.a16, acc);
-            dgo.w[i] = pack_bf16x2(b.dgate.x, b.dgate.y);
-            dlo.w[i] = pack_bf16x2(b.dlin.x, b.dlin.y);
-        } else {
-            situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gv.w[i]), bf16_lo(lv.w[i]), p * g0, c);
-            situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gv.w[i]), bf16_hi(lv.w[i]), p * g1, c);
-            acc.x = fmaf(g0, b0.a16, acc.x);
-            acc.y = fmaf(g1, b1.a16, acc.y);
-            dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
-            dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
-        }
+        float g0 = bf16_lo(yv.w[i]), g1 = bf16_hi(yv.w[i]);
+        situ::Bwd b0 = situ::bwd<BETA4>(bf16_lo(gv.w[i]), bf16_lo(lv.w[i]), p * g0, c);
+        situ::Bwd b1 = situ::bwd<BETA4>(bf16_hi(gv.w[i]), bf16_hi(lv.w[i]), p * g1, c);
+        acc = fmaf(g0, b0.a16, acc);
+        acc = fmaf(g1, b1.a16, acc);
+        dgo.w[i] = pack_bf16x2(b0.dgate, b1.dgate);
+        dlo.w[i] = pack_bf16x2(b0.dlin, b1.dlin);
     }
 }
 
@@ -152,7 +138,7 @@ __global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<S::N
         Vec<NW>* dgr = dx + r * (2 * (int64_t)cpr);
         Vec<NW>* dlr = dgr + cpr;
         const float pr = 16.0f * p[r];   // 16·p: see situ::Bwd
-        float2 acc = situ::pair(0.0f, 0.0f);
+        float acc = 0.0f;
         for (int c0 = 0; c0 < cpr; c0 += 32 * U) {
             Vec<NW> gv[U], lv[U], yv[U];
 #pragma unroll
@@ -169,14 +155,14 @@ __global__ void __launch_bounds__(S::TPB, S::MINB) bwd_vec_kernel(const Vec<S::N
                 const int ci = c0 + k * 32 + lane;
                 if (ci < cpr) {
                     Vec<NW> dgo, dlo;
-                    bwd_chunk<BETA4, NW, S::PAIRED>(gv[k], lv[k], yv[k], pr, c, acc, dgo, dlo);
+                    bwd_chunk<BETA4, NW>(gv[k], lv[k], yv[k], pr, c, acc, dgo, dlo);
                     st_stream<NW>(dgr + ci, dgo);
                     st_stream<NW>(dlr + ci, dlo);
                 }
             }
         }
-        const float sum = warp_sum(acc.x + acc.y);
-        if (lane == 0) dp[r] = 16.0f * sum;
+        acc = warp_sum(acc);
+        if (lane == 0) dp[r] = 16.0f * acc;
     }
 }
 
@@ -228,11 +214,11 @@ struct Fwd16 {       // other H % 8 == 0
 };
 struct Bwd32 {       // H % 16 == 0, 32-byte aligned bases
     static constexpr int NW = 8, U = 1, TPB = 1024, MINB = 1;
-    static constexpr bool NOALLOC = true, PAIRED = false;
+    static constexpr bool NOALLOC = true;
 };
 struct Bwd16 {       // other H % 8 == 0
     static constexpr int NW = 4, U = 2, TPB = 1024, MINB = 1;
-    static constexpr bool NOALLOC = false, PAIRED = false;
+    static constexpr bool NOALLOC = false;
 };
 
 template <bool B4, class S>
