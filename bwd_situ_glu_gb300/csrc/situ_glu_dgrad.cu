@@ -89,7 +89,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* dp_full = (uint64_t*)(dp_cl + 2 * MAX_SPLIT * BM);     // [2] leader: partials of all ranks in
     uint64_t* dp_free = dp_full + 2;                                 // [2] other ranks: the leader read them
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NT = (int)(H / BN);
+    const int NT = (int)((H + BN - 1) / BN);  // the last N-tile may run past H: its extra columns are
+                                              // computed (on the next expert's rows, or zeros past the
+                                              // tensor) and never used
     const uint32_t crank = cluster_rank();
 
     if (threadIdx.x == 0) {
@@ -148,8 +150,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint16_t* dxr = dx + (valid ? row : 0) * 2 * H;
             float acc_dp = 0.0f;
             Vec<8> xb[NBUF][2];                    // [buffer][gate, linear]
-            if (valid) {                           // first chunk: (first N-tile of this CTA, chunk slot)
-                const int64_t j1 = (int64_t)sc.n0 * BN + slot * CW;
+            const int64_t j1 = (int64_t)sc.n0 * BN + slot * CW;
+            if (valid && j1 < H) {                 // first chunk: (first N-tile of this CTA, chunk slot)
                 xb[0][0] = ld_stream<8, true>((const Vec<8>*)(xr + j1));
                 xb[0][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + j1));
             }
@@ -167,12 +169,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const bool last = kk + EPW >= NCH;        // this warp's last chunk of the job
                         // prefetch the next chunk: (nt, kk + EPW), or (next N-tile, slot) after the last
                         if (last) {
-                            if (valid && nt + sc.nstep < NT) {
-                                const int64_t jn = (int64_t)(nt + sc.nstep) * BN + slot * CW;
+                            const int64_t jn = (int64_t)(nt + sc.nstep) * BN + slot * CW;
+                            if (valid && nt + sc.nstep < NT && jn < H) {
                                 xb[0][0] = ld_stream<8, true>((const Vec<8>*)(xr + jn));
                                 xb[0][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn));
                             }
-                        } else if (valid) {
+                        } else if (valid && (int64_t)nt * BN + (kk + EPW) * CW < H) {
                             const int64_t jn = (int64_t)nt * BN + (kk + EPW) * CW;
                             xb[(i + 1) % NBUF][0] = ld_stream<8, true>((const Vec<8>*)(xr + jn));
                             xb[(i + 1) % NBUF][1] = ld_stream<8, true>((const Vec<8>*)(xr + H + jn));
@@ -183,7 +185,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             tc_fence_before();
                             mbar_arrive(&bars->tempty[acc]);     // accumulator may be overwritten
                         }
-                        if (ok && valid) {
+                        if (ok && valid && (int64_t)nt * BN + kk * CW < H) {   // whole chunks: H % 16 == 0
                             const int64_t j0 = (int64_t)nt * BN + kk * CW;
                             Vec<8> dgo, dlo;
 #pragma unroll
@@ -250,8 +252,13 @@ int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const 
                  float lbeta, cudaStream_t stream) {
     int st = check_shape(R, H, beta, lbeta);
     if (st != SITU_GLU_OK) return st;
-    if (D <= 0 || D % BK != 0 || H % BN != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
-    if (R > INT32_MAX || E * H > INT32_MAX || E * D > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
+    // Any H % 16 == 0 (the epilogue's 16-column chunks are whole) and D % 8 == 0 (16-byte TMA row
+    // strides): the last K-block reads zeros past D, the last N-tile computes columns past H that
+    // are never used. The nn.Linear layout keeps D % 64 == 0: its K runs along the rows of
+    // [E·D, H], so a K tail would read the next expert's rows instead of zeros.
+    if (D <= 0 || D % 8 != 0 || H % 16 != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
+    if (w_mn && D % BK != 0) return SITU_GLU_INVALID_ARG;
+    if (R > INT32_MAX || E * H > INT32_MAX - BN || E * D > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
     if (R == 0) return SITU_GLU_OK;
     if (!x || !dy || !w || !expert_offsets || !p || !dx || !dp) return SITU_GLU_INVALID_ARG;
     if (!aligned(x, 32) || !aligned(dy, 16) || !aligned(w, 16) || !aligned(dx, 32) ||
@@ -282,7 +289,7 @@ int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const 
                      : (w_mn ? dgrad_bwd_kernel<false, true> : dgrad_bwd_kernel<false, false>);
     cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int NT = (int)(H / BN);
+    const int NT = (int)((H + BN - 1) / BN);
     const int csplit = NT < DGRAD_SPLIT ? NT : DGRAD_SPLIT;
     const int ncl = (csplit % DGRAD_CLUSTER != 0 || R / E >= CLUSTER4_MIN_ROWS) ? csplit : DGRAD_CLUSTER;
     if (ncl < csplit) {                      // two clusters per M-tile add into dp
@@ -291,7 +298,7 @@ int dgrad_launch(const void* x, const void* dy, const void* w, bool w_mn, const 
     }
     e = launch_clusters(kernel, R, E, ncl, csplit, NUM_THREADS, SMEM_BYTES, stream, map_dy, map_w,
                         (const uint16_t*)x, expert_offsets, p, (uint16_t*)dx, dp, status, (int)E, R, H,
-                        (int)(D / BK), csplit, ncl, c);
+                        (int)((D + BK - 1) / BK), csplit, ncl, c);
     if (e != cudaSuccess) return cuda_fail(e);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);

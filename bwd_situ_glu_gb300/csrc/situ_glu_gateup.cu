@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const Smem sm = carve_smem(smem_raw);
     Barriers* bars = sm.bars;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int NT = (int)(H / HN);
+    const int NT = (int)((H + HN - 1) / HN);   // the last N-tile may run past H: the weight rows past
+                                               // H read as zeros, those columns are never stored
 
     const Sched sc = make_sched(csplit);
     uint32_t tmem;
@@ -141,8 +142,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             mbar_arrive(&bars->tempty[bi]);      // the job's accumulators may be overwritten
                         }
                         static_assert(CW == 16, "one 32-byte vector per output row per chunk");
+                        // whole 16-column chunks (H % 16 == 0): a chunk past H is not evaluated or stored
+                        const bool chunk_ok = (int64_t)nt * HN + k * CW + slot * PAIRS_PER_WARP < H;
                         Vec<8> xg, xl, o;
-                        if (ok && valid) {
+                        if (ok && valid && chunk_ok) {
 #pragma unroll
                             for (int i = 0; i < 8; ++i) {
                                 xg.w[i] = pack_bf16x2(__uint_as_float(gr[2 * i]), __uint_as_float(gr[2 * i + 1]));
@@ -154,7 +157,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                         const int64_t jl = (int64_t)nt * HN + k * CW;                        // within the slice
                         const int64_t j0 = jl + slot * PAIRS_PER_WARP;                       // column in [0, H)
-                        if (ok && full_quad) {
+                        if (ok && full_quad && chunk_ok) {
                             // the warp's 32 rows x CW columns of x (both halves) and of out: staged, then
                             // one TMA store each
                             if (stores_pending) {
@@ -177,7 +180,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                 bulk_commit();
                             }
                             stores_pending = true;
-                        } else if (ok && valid) {
+                        } else if (ok && valid && chunk_ok) {
                             // a quadrant crossing the expert's end: only this row, from registers
                             st_stream<8>((Vec<8>*)(xr + jl), xg);
                             st_stream<8>((Vec<8>*)(xr + H + jl), xl);
@@ -202,7 +205,9 @@ int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* exp
                         cudaStream_t stream) {
     int st = check_shape(R, H, beta, lbeta);
     if (st != SITU_GLU_OK) return st;
-    if (D <= 0 || D % BK != 0 || H % HN != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
+    // Any H % 16 == 0 (whole 16-column epilogue chunks) and D % 8 == 0 (16-byte TMA row strides): the
+    // last K-block reads zeros past D, the last N-tile reads zero weight rows past H.
+    if (D <= 0 || D % 8 != 0 || H % 16 != 0 || E < 1 || E > MAX_EXPERTS) return SITU_GLU_INVALID_ARG;
     if (R > INT32_MAX || E * 2 * H > INT32_MAX || D > INT32_MAX / 2) return SITU_GLU_INVALID_ARG;
     if (R == 0) return SITU_GLU_OK;
     if (!h || !w_gate_up || !expert_offsets || !x || !out) return SITU_GLU_INVALID_ARG;
@@ -238,13 +243,13 @@ int situ_glu_fwd_gateup(const void* h, const void* w_gate_up, const int64_t* exp
                      : (unit2 ? gateup_fwd_kernel<false, 2> : gateup_fwd_kernel<false, 1>);
     cudaError_t e = cudaFuncSetAttribute((const void*)kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_fail(e);
-    const int NT = (int)(H / HN);
+    const int NT = (int)((H + HN - 1) / HN);
     const int csplit = NT < CSPLIT ? NT : CSPLIT;
     int grid = 0;
     if ((e = (cudaError_t)persistent_grid(R, E, csplit, &grid)) != cudaSuccess) return cuda_fail(e);
     kernel<<<grid, NUM_THREADS, SMEM_BYTES, stream>>>(map_h, map_w, map_x, map_out, expert_offsets, (uint16_t*)x,
                                                       (uint16_t*)out,
-                                                      status, (int)E, R, H, (int)(D / BK), csplit, c);
+                                                      status, (int)E, R, H, (int)((D + BK - 1) / BK), csplit, c);
     e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e);
     return SITU_GLU_OK;

@@ -61,7 +61,7 @@ extern "C" {
 #endif
 
 #define SITU_GLU_VERSION_MAJOR 1
-#define SITU_GLU_VERSION_MINOR 5
+#define SITU_GLU_VERSION_MINOR 6
 #define SITU_GLU_VERSION_PATCH 0
 
 /* Largest H accepted (columns per half). */
@@ -184,11 +184,12 @@ int situ_glu_bwd_router_fp8(const uint8_t* xq, const float* xs, const void* g, c
  *              deterministic (that add flushes a subnormal result, |dp| < 2^-126, to zero).
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then dx and dp are incomplete). Zero it beforehand.
- *   R, H, D, E sizes: H % 256 == 0, D % 64 == 0, 1 <= E <= 1024, R < 2^31, E*H < 2^31
+ *   R, H, D, E sizes: H % 16 == 0, D % 8 == 0, 1 <= E <= 1024, R < 2^31, E*H < 2^31 - 256.
+ *              The tensor cores work on 256-column N-tiles and 64-deep K-blocks: a K tail reads
+ *              zeros past D, and an N tail computes columns past H that are never used.
  *   Pointers to dy and w_down_t must be 16-byte aligned (TMA), to x and dx 32-byte aligned
  *   (32-byte vector access).
- * Returns SITU_GLU_INVALID_ARG for shapes or alignments outside these limits (there is no
- * general-shape fallback for this entry point).
+ * Returns SITU_GLU_INVALID_ARG for shapes or alignments outside these limits.
  * --------------------------------------------------------------------------------------- */
 int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_t,
                               const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
@@ -197,8 +198,9 @@ int situ_glu_bwd_router_dgrad(const void* x, const void* dy, const void* w_down_
 
 /* The same with the weights in their nn.Linear layout: w_down device, bf16 [E,D,H], row d of
  * expert e holding W_down,e[d, :], so g[r,j] = Σ_d dy[r,d]·w_down[e,d,j] (read N-major by the
- * tensor cores; no transposed copy needed). E*D < 2^31; everything else as above; results are
- * bit-identical to situ_glu_bwd_router_dgrad on the transposed weights. */
+ * tensor cores; no transposed copy needed). D % 64 == 0 here (K runs along the rows of [E·D, H],
+ * so a K tail would reach the next expert's rows), E*D < 2^31; everything else as above; results
+ * are bit-identical to situ_glu_bwd_router_dgrad on the transposed weights. */
 int situ_glu_bwd_router_dgrad_wd(const void* x, const void* dy, const void* w_down,
                                  const int64_t* expert_offsets, int64_t E, const float* p, void* dx,
                                  float* dp, int* status, int64_t R, int64_t H, int64_t D,
@@ -226,7 +228,9 @@ int situ_glu_bwd_router_dgrad_wd(const void* x, const void* dy, const void* w_do
  *   out        device, bf16 [R,H], written: SiTU-GLU of x
  *   status     device int (may be NULL), written only on failure: set to 1 if a pipeline wait in
  *              the kernel exceeded its limit (then x and out are incomplete). Zero it beforehand.
- *   R, H, D, E sizes: H % 128 == 0, D % 64 == 0, 1 <= E <= 1024, R < 2^31, E*2H < 2^31
+ *   R, H, D, E sizes: H % 16 == 0, D % 8 == 0, 1 <= E <= 1024, R < 2^31, E*2H < 2^31 (the
+ *              tensor cores work on 128-column pairs of N-tiles and 64-deep K-blocks; the tails
+ *              read zeros past H and D, and columns past H are not stored)
  *   Pointers to h and w_gate_up must be 16-byte aligned (TMA), to x and out 32-byte aligned.
  * x and out may not overlap each other or any input (SITU_GLU_OVERLAP). Returns
  * SITU_GLU_INVALID_ARG for shapes or alignments outside these limits.

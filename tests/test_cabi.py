@@ -46,7 +46,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_version_and_status_strings(lib):
-    assert sg.version() == 10500
+    assert sg.version() == 10600
     for s in (0, 1, 2, 3, 99, -1):
         assert isinstance(sg.status_string(s), str) and sg.status_string(s)
     assert sg.status_string(0) == "ok"
@@ -180,8 +180,8 @@ def test_dgrad_validates_before_any_launch(lib):
     dx, dp, st = B, B + (1 << 20), B + (2 << 20)
     args = [x, dy, wt, off, E, p, dx, dp, st]
     assert dgrad(lib, *[None] * 4, E, None, None, None, None, 0, H, D) == OK
-    assert dgrad(lib, *args, R, 128, D) == INVALID                 # H % 256
-    assert dgrad(lib, *args, R, H, 96) == INVALID                  # D % 64
+    assert dgrad(lib, *args, R, 248, D) == INVALID                 # H % 16
+    assert dgrad(lib, *args, R, H, 60) == INVALID                  # D % 8
     assert dgrad(lib, *args, R, H, 0) == INVALID
     assert dgrad(lib, *args, -1, H, D) == INVALID
     assert dgrad(lib, *args, R, H, D, 0.0) == INVALID
@@ -210,9 +210,9 @@ def test_gateup_validates_before_any_launch(lib):
     x, out, st = B, B + (1 << 20), B + (2 << 20)
     args = [h, w, off, E, x, out, st]
     assert gateup(lib, None, None, None, E, None, None, None, 0, H, D) == OK
-    assert gateup(lib, *args, R, 64, D) == INVALID                 # H % 128
-    assert gateup(lib, *args, R, 192, D) == INVALID
-    assert gateup(lib, *args, R, H, 32) == INVALID                 # D % 64
+    assert gateup(lib, *args, R, 120, D) == INVALID                # H % 16
+    assert gateup(lib, *args, R, 8, D) == INVALID
+    assert gateup(lib, *args, R, H, 36) == INVALID                 # D % 8
     assert gateup(lib, *args, -1, H, D) == INVALID
     assert gateup(lib, *args, R, H, D, 4.0, float("nan")) == INVALID
     for bad_e in (0, -1, 4097):
@@ -246,7 +246,7 @@ def test_dgrad_wd_validates_before_any_launch(lib):
     dx, dp, st = B, B + (1 << 20), B + (2 << 20)
     f = lambda *a: lib.situ_glu_bwd_router_dgrad_wd(*a, None)
     assert f(None, None, None, None, E, None, None, None, None, 0, H, D, 4.0, 25.0) == OK
-    assert f(x, dy, w, off, E, p, dx, dp, st, R, 128, D, 4.0, 25.0) == INVALID          # H % 256
-    assert f(x, dy, w, off, E, p, dx, dp, st, R, H, 96, 4.0, 25.0) == INVALID           # D % 64
+    assert f(x, dy, w, off, E, p, dx, dp, st, R, 248, D, 4.0, 25.0) == INVALID          # H % 16
+    assert f(x, dy, w, off, E, p, dx, dp, st, R, H, 96, 4.0, 25.0) == INVALID           # D % 64 (nn.Linear layout)
     assert f(x, dy, w + 8, off, E, p, dx, dp, st, R, H, D, 4.0, 25.0) == INVALID        # w 16-byte aligned
     assert f(x, dy, w, off, E, p, w + 64, dp, st, R, H, D, 4.0, 25.0) == OVERLAP        # dx over w

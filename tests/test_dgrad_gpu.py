@@ -54,6 +54,13 @@ CASES = {
     # either side of the host's choice (experts averaging 512 rows or more: one cluster of 4)
     "cluster_choice_511": ([510, 512], 1024, 64),
     "cluster_choice_512": ([512, 512], 1024, 64),
+    # shapes off the 256-column N-tile and 64-deep K-block grid (H % 16 == 0, D % 8 == 0): the last
+    # N-tile computes columns past H that are never used, the last K-block reads zeros past D
+    "n_tail_h272": ([200, 77, 0, 129], 272, 128),
+    "k_tail_d72": ([150, 300], 512, 72),
+    "smallest_h16_d8": ([33, 0, 100], 16, 8),
+    "both_tails_h1040_d200": ([300, 292, 250], 1040, 200),
+    "both_tails_large_experts": ([600, 700], 400, 136),
 }
 
 
@@ -239,7 +246,8 @@ def test_dgrad_dp_is_deterministic(sg):
         assert torch.equal(dp.view(torch.int32), runs[0][1].view(torch.int32))
 
 
-@pytest.mark.parametrize("name", ["partial_tiles", "empty_experts", "uneven_split", "real_widths", "large_experts"])
+@pytest.mark.parametrize("name", ["partial_tiles", "empty_experts", "uneven_split", "real_widths", "large_experts",
+                                  "n_tail_h272"])
 def test_dgrad_nn_linear_weight_layout(sg, name):
     """W_down in its nn.Linear layout [E, D, H] (read N-major by the tensor cores) gives exactly
     the results of the transposed weights [E, H, D]; and both match the oracle."""

@@ -87,6 +87,13 @@ CASES = {
     # either side of the host's choice (experts averaging 512 rows or more: two-tile units)
     "unit_choice_511": ([510, 512], 256, 64),
     "unit_choice_512": ([512, 512], 256, 64),
+    # shapes off the 128-column-pair N-tile and 64-deep K-block grid (H % 16 == 0, D % 8 == 0): the
+    # weight rows past H and the K columns past D read as zeros, chunks past H are not stored
+    "n_tail_h144": ([100, 60, 0], 144, 64),
+    "k_tail_d200": ([200, 0, 129], 256, 200),
+    "smallest_h16_d8": ([40, 1], 16, 8),
+    "both_tails_h1040_d72": ([300, 292], 1040, 72),
+    "both_tails_two_tile_units": ([600, 700], 400, 136),
 }
 
 
@@ -131,8 +138,10 @@ def test_gateup_matches_unfused_path(sg):
 
 def test_gateup_rejects_unsupported_shapes(sg):
     h, w, off = make([64], 128, 64, seed=1)
-    with pytest.raises(sg.SituGluError):                  # H = 96 is not a multiple of 128
-        sg.situ_glu_fwd_gateup(h.to(DEV), w.to(DEV)[:, :192].contiguous(), off.to(DEV))
+    with pytest.raises(sg.SituGluError):                  # H = 100 is not a multiple of 16
+        sg.situ_glu_fwd_gateup(h.to(DEV), w.to(DEV)[:, :200].contiguous(), off.to(DEV))
+    with pytest.raises(sg.SituGluError):                  # D = 60 is not a multiple of 8
+        sg.situ_glu_fwd_gateup(h.to(DEV)[:, :60].contiguous(), w.to(DEV)[:, :, :60].contiguous(), off.to(DEV))
 
 
 @pytest.mark.slow
